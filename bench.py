@@ -1,0 +1,415 @@
+"""Benchmark: one training-step pass of the NVFP4 MLP hot path on a B300.
+
+A step is the whole hot path over one batch of synthetic input, for the
+Llama 3 8B MLP at 32768 tokens (sequence 8192 x batch 4):
+  fprop : X [32768, 4096] 1D RNE, gate+up W [28672, 4096] 2D  -> Y = X W^T
+  dgrad : dY [32768, 14336] 1D SR, W [14336, 4096] 2D transposed -> dX = dY W
+  wgrad : dY^T and X^T with the 16-point RHT + SR (same RHT seed)  -> dW = dY^T X
+i.e. 6 quantisations (amax pass + encode each) and 3 block-scaled GEMMs.
+
+Printed metric: NVFP4 GEMM TFLOP/s of the step (GEMM flops / step time,
+quantisation included) on rank 0, one JSON line.  Kernel-level numbers (GEMM
+TFLOP/s, quantiser GB/s) and the roofline of the dominant kernel are in the
+same line.  `--impl reference` times the CPU oracle on a bounded sample of
+the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import (LLAMA3_8B_DY, LLAMA3_8B_FPROP, LLAMA3_8B_W_BWD, RHT_SEED,  # noqa: E402
+                       make_bf16, sr_seed)
+
+T, H, F2, F = 32768, 4096, 28672, 14336
+GEMM_FLOPS = {"fprop": 2.0 * T * F2 * H, "dgrad": 2.0 * T * H * F, "wgrad": 2.0 * F * H * T}
+STEP_FLOPS = sum(GEMM_FLOPS.values())
+WORKLOAD = "llama3-8b-mlp fprop+dgrad+wgrad, tokens 32768 (seq 8192 x batch 4), hidden 4096, ffn 14336"
+
+# algorithmic bytes of one quantisation of an [r, c] bf16 tensor:
+# read 2 B/elem, write 0.5 B codes + 1/16 B scales
+QUANT_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 16.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class MlpStep:
+    """Device buffers and the launch sequence of one fwd+bwd MLP step."""
+
+    def __init__(self, nv, device):
+        self.nv = nv
+        self.dev = device
+        self.x = make_bf16(LLAMA3_8B_FPROP.a, device=device)   # [T, H]
+        self.w = make_bf16(LLAMA3_8B_FPROP.b, device=device)   # [F2, H]
+        self.dy = make_bf16(LLAMA3_8B_DY, device=device)       # [T, F]
+        self.w2 = make_bf16(LLAMA3_8B_W_BWD, device=device)    # [F, H]
+        e = nv.empty_nvfp4
+        self.qx = e(T, H, device=device)
+        self.qw = e(F2, H, device=device)
+        self.qdy = e(T, F, device=device)
+        self.qw2t = e(H, F, device=device)
+        self.qdyt = e(F, T, device=device)
+        self.qxt = e(H, T, device=device)
+        self.y = torch.empty(T, F2, dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty(F, H, dtype=torch.bfloat16, device=device)
+        self.launches_per_step = 6 * 2 + 3
+
+    def run(self, stream, gemm_events=None, quant_events=None):
+        nv = self.nv
+
+        def q(ev_i, fn):
+            if quant_events is not None:
+                quant_events[ev_i][0].record(stream)
+            fn()
+            if quant_events is not None:
+                quant_events[ev_i][1].record(stream)
+
+        def g(ev_i, a, b, c):
+            if gemm_events is not None:
+                gemm_events[ev_i][0].record(stream)
+            nv.nvfp4_gemm(a, b, c, stream)
+            if gemm_events is not None:
+                gemm_events[ev_i][1].record(stream)
+
+        # fprop
+        q(0, lambda: nv.nvfp4_quantize(self.x, nv.BLOCK_1D, 0, None, self.qx, stream))
+        q(1, lambda: nv.nvfp4_quantize(self.w, nv.BLOCK_2D, 0, None, self.qw, stream))
+        g(0, self.qx, self.qw, self.y)
+        # dgrad
+        q(2, lambda: nv.nvfp4_quantize(self.dy, nv.ROUND_SR, sr_seed(0), None, self.qdy, stream))
+        q(3, lambda: nv.nvfp4_quantize(self.w2, nv.BLOCK_2D | nv.TRANSPOSE_OUT, 0, None, self.qw2t, stream))
+        g(1, self.qdy, self.qw2t, self.dx)
+        # wgrad
+        q(4, lambda: nv.nvfp4_quantize_rht_sr(self.dy, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(1), None, self.qdyt,
+                                             stream))
+        q(5, lambda: nv.nvfp4_quantize_rht_sr(self.x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(2), None, self.qxt,
+                                             stream))
+        g(2, self.qdyt, self.qxt, self.dw)
+
+    quant_elems = [T * H, F2 * H, T * F, F * H, T * F, T * H]
+    quant_names = ["X 1D", "W 2D", "dY 1D SR", "W^T 2D", "dY^T RHT+SR", "X^T RHT+SR"]
+
+
+def run_ours(args):
+    import nvfp4_block_scaled_27_b300 as nv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    nv.load_library()
+    stream = torch.cuda.Stream(device=device)
+    step = MlpStep(nv, device)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.run(stream)
+    stream.synchronize()
+    nv.check_status(stream)
+
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(6)]
+    gemm_ev = [mk()[:3] for _ in range(args.steps)]
+    quant_ev = [mk() for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                step.run(stream, gemm_ev[k], quant_ev[k])
+        t1.record(stream)
+        stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    nv.check_status(stream)
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+
+    gemm_ms = {n: statistics.mean(gemm_ev[k][i][0].elapsed_time(gemm_ev[k][i][1]) for k in range(args.steps))
+               for i, n in enumerate(["fprop", "dgrad", "wgrad"])}
+    quant_ms = [statistics.mean(quant_ev[k][i][0].elapsed_time(quant_ev[k][i][1]) for k in range(args.steps))
+                for i in range(6)]
+    gemm_total_ms = sum(gemm_ms.values())
+    gemm_tflops = STEP_FLOPS / (gemm_total_ms * 1e-3) / 1e12
+    quant_bytes = sum(QUANT_BYTES_PER_ELEM * n for n in step.quant_elems)
+    quant_gbs = quant_bytes / (sum(quant_ms) * 1e-3) / 1e9
+
+    peaks, peak_src = _peaks()
+    fp4_burst = peaks["bf16_tflops"] * (13.5 / 2.25)
+    fp4_sust = peaks["bf16_tflops_sustained"] * (13.5 / 2.25)
+    traffic = _committed_traffic()
+
+    value = world * STEP_FLOPS / (ms_step * 1e-3) / 1e12
+    e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    clocks = clk.summary()
+
+    if rank == 0:
+        line = {
+            "metric": "NVFP4 GEMM TFLOP/s over an MLP fwd+bwd step (quantisation included)",
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e4m3 x fp32) -> fp32 accumulate -> bf16",
+            "data": "synthetic (seeded Gaussian with outliers; shapes of the Llama 3 8B MLP)",
+            "config": {"workload": WORKLOAD, "tokens": T, "hidden": H, "ffn": F, "gate_up": F2,
+                       "l2": "inputs larger than L2 (X 256 MiB, dY 896 MiB per step)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "gemm": {n: {"ms": round(v, 4), "tflops": round(GEMM_FLOPS[n] / (v * 1e-3) / 1e12, 1)}
+                     for n, v in gemm_ms.items()},
+            "quantize": [{"tensor": nm, "ms": round(t, 4),
+                          "gbs": round(QUANT_BYTES_PER_ELEM * n / (t * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(QUANT_BYTES_PER_ELEM * n / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+                         for nm, n, t in zip(step.quant_names, step.quant_elems, quant_ms)],
+            "quantize_gbs_all": round(quant_gbs, 1),
+            "roofline": {"kernel": "nvfp4_gemm_kernel", "bound": "tensor", "achieved": round(gemm_tflops, 1),
+                         "peak": round(fp4_burst, 1), "unit": "TFLOP/s",
+                         "frac": round(gemm_tflops / fp4_burst, 4),
+                         "peak_note": f"{peak_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal fp4/bf16 ratio)",
+                         "frac_of_sustained": round(gemm_tflops / fp4_sust, 4),
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": step.launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _committed_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                return json.load(f).get("bytes_per_launch")
+        except (OSError, ValueError):
+            return None
+    return None
+
+
+def run_e2e(nv, step, stream, device, args):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in, results copied out, inside the timed region."""
+    hx = step.x.cpu().pin_memory()
+    hw = step.w.cpu().pin_memory()
+    hdy = step.dy.cpu().pin_memory()
+    hw2 = step.w2.cpu().pin_memory()
+    hy = torch.empty(step.y.shape, dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty(step.dx.shape, dtype=torch.bfloat16).pin_memory()
+    hdw = torch.empty(step.dw.shape, dtype=torch.bfloat16).pin_memory()
+    ins = [(step.x, hx), (step.w, hw), (step.dy, hdy), (step.w2, hw2)]
+    outs = [(step.y, hy), (step.dx, hdx), (step.dw, hdw)]
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+    stream.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            one()
+    t1.record(stream)
+    stream.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    bi = sum(h.numel() * h.element_size() for _, h in ins)
+    bo = sum(h.numel() * h.element_size() for _, h in outs)
+    return {"value": round(STEP_FLOPS / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps}
+
+
+# --------------------------------------------------------------- oracle --
+def _oracle_sample(rows_a=8, cols_n=256):
+    """Oracle work for a bounded slice of the step: quantise `rows_a` token
+    rows and `cols_n` weight rows for each of the three GEMMs and evaluate
+    those rows x cols outputs in fp64.  Returns (flops of the slice, s)."""
+    import numpy as np
+
+    import oracle as o
+    from workloads import LLAMA3_8B_X_BWD, TensorSpec, bf16_bits
+
+    def slab(spec, rows):
+        return bf16_bits(make_bf16(TensorSpec(rows, spec.cols, spec.std, spec.outlier_p, spec.outlier_factor,
+                                              spec.seed), device="cpu"))
+
+    t = time.time()
+    flops = 0.0
+    # fprop slice: X rows x W rows, K = 4096
+    qa = o.quantize(slab(LLAMA3_8B_FPROP.a, rows_a), 0)
+    qb = o.quantize(slab(LLAMA3_8B_FPROP.b, cols_n), o.FLAG_BLOCK_2D)
+    o.gemm(qa, qb)
+    flops += 2.0 * rows_a * cols_n * H
+    # dgrad slice: dY rows x W^T rows (W [F, H] -> W^T rows are H), K = F
+    qdy = o.quantize(slab(LLAMA3_8B_DY, rows_a), o.FLAG_SR, sr_seed=sr_seed(0))
+    w2 = slab(LLAMA3_8B_W_BWD, F)[:, :cols_n]
+    qw2t = o.quantize(np.ascontiguousarray(w2), o.FLAG_BLOCK_2D | o.FLAG_TRANSPOSE)
+    o.gemm(qdy, qw2t)
+    flops += 2.0 * rows_a * cols_n * F
+    # wgrad slice: contraction over a token slab of 16 * rows_a tokens
+    tok = 16 * rows_a
+    qdyt = o.quantize(slab(LLAMA3_8B_DY, tok)[:, :cols_n].copy(), o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE,
+                      rht_seed=RHT_SEED, sr_seed=sr_seed(1))
+    qxt = o.quantize(slab(LLAMA3_8B_X_BWD, tok)[:, :cols_n].copy(), o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE,
+                     rht_seed=RHT_SEED, sr_seed=sr_seed(2))
+    o.gemm(qdyt, qxt)
+    flops += 2.0 * cols_n * cols_n * tok
+    return flops, time.time() - t
+
+
+def cpu_baseline(args, rows_a=32, cols_n=512):
+    import oracle as o
+    o.build()
+    flops, secs = _oracle_sample(rows_a, cols_n)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": o.get_threads(), "kind": "oracle",
+            "sample": f"fprop/dgrad/wgrad slices: {rows_a} token rows x {cols_n} output columns each "
+                      f"(quantisation of those operand rows included), {secs:.1f} s",
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as o
+    o.build()
+    for _ in range(args.warmup):
+        _oracle_sample(2, 64)
+    t = time.time()
+    flops = 0.0
+    for _ in range(args.steps):
+        f, _ = _oracle_sample(2, 64)
+        flops += f
+    secs = time.time() - t
+    v = flops / secs / 1e12
+    line = {"impl": "reference", "metric": "NVFP4 GEMM TFLOP/s over an MLP fwd+bwd step (quantisation included)",
+            "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp64 oracle over nvfp4 operands", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "2 token rows x 64 output columns per GEMM per step"},
+            "cpu_baseline": {"kind": "oracle", "cores": o.get_threads(), "value": v, "unit": "TFLOP/s",
+                             "sample": "2 token rows x 64 output columns per GEMM per step"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * nvfp4.h -- C ABI of the B300 (sm_103a) NVFP4 quantisation and block-scaled
+ * NVFP4 GEMM library.
+ *
+ * What the library computes, with the passages that define it:
+ *   - NVFP4 is a two-level micro-scaled 4-bit format: E2M1 elements (1 sign,
+ *     2 exponent, 1 mantissa bit), one FP8 E4M3 scale per 16 consecutive
+ *     elements, and one FP32 scale for the whole tensor.
+ *       "NVFP4: cos'è e come supera FP8 e BF16 nell'intelligenza artificiale"
+ *       (guiahardware.es), section "Cos'è NVFP4 e in che modo migliora FP8 e
+ *       BF16?"; "FP4" (chaitex.ru/fp4), section "Математическая структура
+ *       FP4", items 1-2; "Mastering Low-Precision AI: FP8 and FP4 Support
+ *       Across Frameworks in Mid-2026", first paragraph.
+ *   - The training recipe uses NVFP4 for the three GEMMs of each MLP layer
+ *     (fprop, dgrad, wgrad), all with NVFP4 operands and BF16 results; weights
+ *     use 2D (16x16) blocks so that quantising W and W^T agree; the wgrad
+ *     operands get a random Hadamard transform before quantisation; gradient
+ *     quantisers use stochastic rounding.
+ *       readjensen.com NVFP4 training-recipe article (2026-06-08), paragraphs
+ *       on the recipe and on the data flow inside the MLP GEMMs.
+ *
+ * Numeric definition (every step IEEE fp32 round-to-nearest-even):
+ *   amax  = max |x| over the tensor (over the transformed values with RHT)
+ *   s_g   = amax / 2688                      (2688 = 6 * 448)
+ *   block : sc = E4M3_RNE_satfinite(amax_b / (s_g * 6)), 0 if s_g == 0
+ *   elem  : v = x * (1 / (s_g * decode(sc))) (0 if decode(sc) == 0);
+ *           code = E2M1 round-to-nearest-even (or stochastic), saturating at
+ *           +-6, sign bit kept (negative values that round to 0 give 0x8)
+ *   RHT   : y = 1/4 * H16 * (d (.) x) per 16-chunk along the quantisation axis,
+ *           Sylvester H16, d_j = -1 iff bit j of mix32(key(rht_seed, 0x5248))
+ *   SR    : round |v| up iff u16 * 2^-16 < (|v| - lo) / (hi - lo); u16 comes
+ *           from the lowbias32 hash of (sr_seed, output element index)
+ *   GEMM  : C[m,n] = bf16_rne( s_gA * s_gB * sum_k A[m,k] * B[n,k] ), fp32
+ *           accumulation on the tensor cores.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers unless stated.  The caller owns all
+ *     memory; the library allocates nothing and keeps no reference after the
+ *     call returns.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL means
+ *     the legacy default stream).  Errors found on the host are returned
+ *     immediately and nothing is launched.  Errors found on the device (a
+ *     bounded wait that expired, a non-finite amax) set a per-device status
+ *     word that nvfp4_check_status() reads and clears.
+ *   - Shapes use int64_t; a NVFP4 operand [rows, cols] is quantised along
+ *     cols (the GEMM contraction dimension K).
+ */
+#ifndef NVFP4_B300_H
+#define NVFP4_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t; /* same type as cudaStream_t */
+
+/* ---- status codes ------------------------------------------------------- */
+#define NVFP4_OK 0
+#define NVFP4_ERR_INVALID_ARG (-1) /* null pointer, bad shape, misalignment  */
+#define NVFP4_ERR_UNSUPPORTED (-2) /* device is not sm_100-family / sm_103a  */
+#define NVFP4_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed    */
+#define NVFP4_ERR_TIMEOUT (-4)     /* a bounded device-side wait expired      */
+#define NVFP4_ERR_NONFINITE (-5)   /* an input tensor held NaN or Inf         */
+
+/* ---- quantiser flags ---------------------------------------------------- */
+#define NVFP4_BLOCK_1D 0x0u       /* 16 consecutive elements along a row     */
+#define NVFP4_BLOCK_2D 0x1u       /* aligned 16x16 tiles (weights)           */
+#define NVFP4_ROUND_RNE 0x0u      /* round to nearest even                   */
+#define NVFP4_ROUND_SR 0x2u       /* stochastic rounding                     */
+#define NVFP4_TRANSPOSE_OUT 0x4u  /* quantise x^T: output is [cols, rows]    */
+
+/* ---- scale-factor layouts ------------------------------------------------ */
+/* CANONICAL: row-major [rows, cols/16] bytes.
+ * MMA: the layout the GEMM consumes.  Rows are padded to a multiple of 128
+ * and cols must be a multiple of 64.  For row r and 16-element block kb the
+ * byte offset is
+ *     ((r / 128) * (cols / 64) + kb / 4) * 512
+ *   + (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4,
+ * i.e. one 512-byte atom per (128 rows, 64 columns) holding 4 scales per
+ * row, row r's 4-byte word at (r % 32, r / 32).  Padding rows read as 0. */
+#define NVFP4_SCALES_CANONICAL 0
+#define NVFP4_SCALES_MMA 1
+
+/* A quantised operand.  All buffers are device memory owned by the caller.
+ *   codes        [rows, cols/2] bytes: element 2j in the low nibble of byte j.
+ *   scales       E4M3 block scales (sign bit 0) in `scale_layout`;
+ *                nvfp4_scales_bytes() gives the size.
+ *   amax         fp32 scalar, written by the quantiser.
+ *   global_scale fp32 scalar s_g, written by the quantiser, read by the GEMM.
+ *   rows, cols   logical shape of the quantised operand (cols = K). */
+typedef struct nvfp4_tensor {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* amax;
+  float* global_scale;
+  int64_t rows;
+  int64_t cols;
+  int32_t scale_layout;
+  int32_t reserved; /* must be 0 */
+} nvfp4_tensor;
+
+/* Bytes of the scale buffer for an operand [rows, cols] in `layout`
+ * (0 for an invalid combination). */
+size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t layout);
+
+/* Quantise a bf16 matrix x [rows, cols] (row stride ld elements) to NVFP4.
+ * flags: NVFP4_BLOCK_1D or NVFP4_BLOCK_2D, NVFP4_ROUND_RNE or NVFP4_ROUND_SR,
+ * optionally NVFP4_TRANSPOSE_OUT (then out is [cols, rows], blocks run along
+ * the input's rows).  out->rows/out->cols must equal the output shape.
+ * sr_seed keys the stochastic rounding (ignored for RNE).  amax_in (device
+ * fp32, nullable) supplies the tensor amax and skips the amax pass.
+ * Requirements: x 16-byte aligned, ld % 8 == 0, cols % 8 == 0, the output's
+ * cols % 16 == 0 (and % 64 for the MMA scale layout), both output dims % 16
+ * for 2D.  Returns NVFP4_OK or a negative status code. */
+int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                   uint32_t flags, uint64_t sr_seed, const float* amax_in,
+                   const nvfp4_tensor* out, nvfp4_stream_t stream);
+
+/* Quantise with the 16-point random Hadamard transform and stochastic
+ * rounding (the wgrad operands).  The transform runs along the output's
+ * quantisation axis, so with NVFP4_TRANSPOSE_OUT (the usual wgrad case) it
+ * mixes 16 consecutive rows (tokens) of x.  Both wgrad operands must use the
+ * same rht_seed; use different sr_seeds.  The amax is taken after the
+ * transform.  NVFP4_BLOCK_2D is not allowed; other arguments as for
+ * nvfp4_quantize(). */
+int nvfp4_quantize_rht_sr(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                          uint32_t flags, uint64_t rht_seed, uint64_t sr_seed,
+                          const float* amax_in, const nvfp4_tensor* out,
+                          nvfp4_stream_t stream);
+
+/* Block-scaled NVFP4 GEMM, "TN": C[M, N] = s_gA * s_gB * A[M, K] * B[N, K]^T
+ * with fp32 accumulation and a BF16 (round-to-nearest-even) result.
+ * A and B must use NVFP4_SCALES_MMA, K = A->cols = B->cols, K % 256 == 0.
+ * c is bf16 [M, N] with row stride ldc elements (ldc >= N, ldc % 8 == 0,
+ * c 16-byte aligned).  The same call serves fprop (X * W^T), dgrad
+ * (dY * (W^T)^T) and wgrad (dY^T * (X^T)^T) given suitably quantised operands. */
+int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc,
+               nvfp4_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device status word of the
+ * current device.  Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, NVFP4_ERR_NONFINITE
+ * or NVFP4_ERR_CUDA. */
+int nvfp4_check_status(nvfp4_stream_t stream);
+
+/* Static description of a status code. */
+const char* nvfp4_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int nvfp4_version(void);
+
+/* ---- codec diagnostics (exhaustive conversion checks) -------------------- */
+/* out[i] = E2M1 code (low nibble) of v[i] with round-to-nearest-even,
+ * saturating, sign kept -- the element encoder the quantiser uses.
+ * v and out are device arrays of n elements. */
+int nvfp4_encode_e2m1_rne(const float* v, int64_t n, uint8_t* out, nvfp4_stream_t stream);
+
+/* out[i] = E2M1 code of v[i] rounded stochastically with the 16 random bits
+ * u16[i] (the quantiser's SR encoder). */
+int nvfp4_encode_e2m1_sr(const float* v, const uint16_t* u16, int64_t n, uint8_t* out,
+                         nvfp4_stream_t stream);
+
+/* out[i] = E4M3 code of t[i] >= 0, round-to-nearest-even, saturating at 448,
+ * NaN -> 0 (the quantiser's block-scale encoder). */
+int nvfp4_encode_e4m3(const float* t, int64_t n, uint8_t* out, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_B300_H */

@@ -1,0 +1,246 @@
+"""Python binding of the NVFP4 C ABI (``include/nvfp4.h``).
+
+Argument marshalling only: torch tensors provide device memory and the
+current CUDA stream; every step of quantisation and the GEMM runs in the
+library's CUDA kernels (``libnvfp4_b300.so``, sm_103a).  There is no CPU
+fallback: importing works without a GPU (for the build check and the symbol
+test), but every compute call raises if the library or a CUDA device is
+missing.
+
+Low-level functions keep the C names (``nvfp4_quantize``,
+``nvfp4_quantize_rht_sr``, ``nvfp4_gemm``, ``nvfp4_check_status`` ...);
+``quantize``/``quantize_rht_sr``/``gemm`` are thin helpers that allocate the
+outputs with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4_b300.so")
+
+# status codes
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_TIMEOUT = -4
+ERR_NONFINITE = -5
+
+# flags
+BLOCK_1D = 0x0
+BLOCK_2D = 0x1
+ROUND_RNE = 0x0
+ROUND_SR = 0x2
+TRANSPOSE_OUT = 0x4
+
+SCALES_CANONICAL = 0
+SCALES_MMA = 1
+
+EXPORTED = (
+    "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_gemm",
+    "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
+    "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3",
+)
+
+
+class Nvfp4Error(RuntimeError):
+    pass
+
+
+class CTensor(ctypes.Structure):
+    """Mirror of ``nvfp4_tensor``."""
+    _fields_ = [
+        ("codes", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("amax", ctypes.c_void_p),
+        ("global_scale", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("scale_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise Nvfp4Error(f"CUDA library not built: {path} (run python -m nvfp4_block_scaled_27_b300._build)")
+    L = ctypes.CDLL(path)
+    vp, i64, u32, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int32
+    tp = ctypes.POINTER(CTensor)
+    L.nvfp4_scales_bytes.restype = ctypes.c_size_t
+    L.nvfp4_scales_bytes.argtypes = [i64, i64, i32]
+    L.nvfp4_quantize.restype = ctypes.c_int
+    L.nvfp4_quantize.argtypes = [vp, i64, i64, i64, u32, u64, vp, tp, vp]
+    L.nvfp4_quantize_rht_sr.restype = ctypes.c_int
+    L.nvfp4_quantize_rht_sr.argtypes = [vp, i64, i64, i64, u32, u64, u64, vp, tp, vp]
+    L.nvfp4_gemm.restype = ctypes.c_int
+    L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, vp]
+    L.nvfp4_check_status.restype = ctypes.c_int
+    L.nvfp4_check_status.argtypes = [vp]
+    L.nvfp4_status_string.restype = ctypes.c_char_p
+    L.nvfp4_status_string.argtypes = [ctypes.c_int]
+    L.nvfp4_version.restype = ctypes.c_int
+    L.nvfp4_version.argtypes = []
+    L.nvfp4_encode_e2m1_rne.restype = ctypes.c_int
+    L.nvfp4_encode_e2m1_rne.argtypes = [vp, i64, vp, vp]
+    L.nvfp4_encode_e2m1_sr.restype = ctypes.c_int
+    L.nvfp4_encode_e2m1_sr.argtypes = [vp, vp, i64, vp, vp]
+    L.nvfp4_encode_e4m3.restype = ctypes.c_int
+    L.nvfp4_encode_e4m3.argtypes = [vp, i64, vp, vp]
+    _lib = L
+    return L
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        msg = load_library().nvfp4_status_string(rc).decode()
+        raise Nvfp4Error(f"{what} failed: {rc} ({msg})")
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _require_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda:
+            raise Nvfp4Error("tensors must live on a CUDA device (no CPU path)")
+
+
+@dataclass
+class NVFP4Tensor:
+    """A quantised operand in device memory (see ``nvfp4_tensor``)."""
+    codes: torch.Tensor         # uint8 [rows, cols/2]
+    scales: torch.Tensor        # uint8, nvfp4_scales_bytes(rows, cols, layout)
+    amax: torch.Tensor          # float32 [1]
+    global_scale: torch.Tensor  # float32 [1]
+    rows: int
+    cols: int
+    scale_layout: int = SCALES_MMA
+
+    def c_struct(self) -> CTensor:
+        return CTensor(self.codes.data_ptr(), self.scales.data_ptr(), self.amax.data_ptr(),
+                       self.global_scale.data_ptr(), self.rows, self.cols, self.scale_layout, 0)
+
+    @property
+    def shape(self):
+        return (self.rows, self.cols)
+
+
+def scales_bytes(rows: int, cols: int, layout: int) -> int:
+    return int(load_library().nvfp4_scales_bytes(rows, cols, layout))
+
+
+def empty_nvfp4(rows: int, cols: int, layout: int = SCALES_MMA, device="cuda") -> NVFP4Tensor:
+    n = scales_bytes(rows, cols, layout)
+    if n == 0 and rows * cols != 0:
+        raise Nvfp4Error(f"invalid shape ({rows}, {cols}) for scale layout {layout}")
+    return NVFP4Tensor(
+        codes=torch.empty((rows, cols // 2), dtype=torch.uint8, device=device),
+        scales=torch.empty((max(n, 1),), dtype=torch.uint8, device=device),
+        amax=torch.empty((1,), dtype=torch.float32, device=device),
+        global_scale=torch.empty((1,), dtype=torch.float32, device=device),
+        rows=rows, cols=cols, scale_layout=layout)
+
+
+# ------------------------------------------------------------ raw C calls --
+def nvfp4_quantize(x: torch.Tensor, flags: int, sr_seed: int, amax_in, out: NVFP4Tensor, stream=None) -> None:
+    _require_cuda(x)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise Nvfp4Error("x must be a 2-D bf16 tensor with unit column stride")
+    ct = out.c_struct()
+    rc = load_library().nvfp4_quantize(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), flags, sr_seed,
+                                       None if amax_in is None else amax_in.data_ptr(), ctypes.byref(ct),
+                                       _stream(stream))
+    _check(rc, "nvfp4_quantize")
+
+
+def nvfp4_quantize_rht_sr(x: torch.Tensor, flags: int, rht_seed: int, sr_seed: int, amax_in, out: NVFP4Tensor,
+                          stream=None) -> None:
+    _require_cuda(x)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise Nvfp4Error("x must be a 2-D bf16 tensor with unit column stride")
+    ct = out.c_struct()
+    rc = load_library().nvfp4_quantize_rht_sr(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), flags, rht_seed,
+                                              sr_seed, None if amax_in is None else amax_in.data_ptr(),
+                                              ctypes.byref(ct), _stream(stream))
+    _check(rc, "nvfp4_quantize_rht_sr")
+
+
+def nvfp4_gemm(a: NVFP4Tensor, b: NVFP4Tensor, c: torch.Tensor, stream=None) -> None:
+    _require_cuda(c)
+    if c.dtype != torch.bfloat16 or c.dim() != 2 or c.stride(1) != 1:
+        raise Nvfp4Error("c must be a 2-D bf16 tensor with unit column stride")
+    ca, cb = a.c_struct(), b.c_struct()
+    rc = load_library().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), c.data_ptr(), c.stride(0),
+                                   _stream(stream))
+    _check(rc, "nvfp4_gemm")
+
+
+def nvfp4_check_status(stream=None) -> int:
+    return int(load_library().nvfp4_check_status(_stream(stream)))
+
+
+def nvfp4_encode_e2m1_rne(v: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _require_cuda(v, out)
+    _check(load_library().nvfp4_encode_e2m1_rne(v.data_ptr(), v.numel(), out.data_ptr(), _stream(stream)),
+           "nvfp4_encode_e2m1_rne")
+
+
+def nvfp4_encode_e2m1_sr(v: torch.Tensor, u16: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _require_cuda(v, u16, out)
+    _check(load_library().nvfp4_encode_e2m1_sr(v.data_ptr(), u16.data_ptr(), v.numel(), out.data_ptr(),
+                                               _stream(stream)), "nvfp4_encode_e2m1_sr")
+
+
+def nvfp4_encode_e4m3(t: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _require_cuda(t, out)
+    _check(load_library().nvfp4_encode_e4m3(t.data_ptr(), t.numel(), out.data_ptr(), _stream(stream)),
+           "nvfp4_encode_e4m3")
+
+
+# ---------------------------------------------------------------- helpers --
+def quantize(x: torch.Tensor, flags: int = 0, sr_seed: int = 0, amax_in=None, layout: int = SCALES_MMA,
+             out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
+    rows, cols = x.shape
+    orows, ocols = (cols, rows) if flags & TRANSPOSE_OUT else (rows, cols)
+    if out is None:
+        out = empty_nvfp4(orows, ocols, layout, x.device)
+    nvfp4_quantize(x, flags, sr_seed, amax_in, out, stream)
+    return out
+
+
+def quantize_rht_sr(x: torch.Tensor, flags: int = TRANSPOSE_OUT, rht_seed: int = 0, sr_seed: int = 0,
+                    amax_in=None, layout: int = SCALES_MMA, out: NVFP4Tensor | None = None,
+                    stream=None) -> NVFP4Tensor:
+    rows, cols = x.shape
+    orows, ocols = (cols, rows) if flags & TRANSPOSE_OUT else (rows, cols)
+    if out is None:
+        out = empty_nvfp4(orows, ocols, layout, x.device)
+    nvfp4_quantize_rht_sr(x, flags, rht_seed, sr_seed, amax_in, out, stream)
+    return out
+
+
+def gemm(a: NVFP4Tensor, b: NVFP4Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.codes.device)
+    nvfp4_gemm(a, b, out, stream)
+    return out
+
+
+def check_status(stream=None) -> None:
+    _check(nvfp4_check_status(stream), "device status")

@@ -1,0 +1,319 @@
+// nvfp4_device.cuh -- device helpers shared by the library's kernels:
+// element/scale codecs, the counter hash, the 16-point transform, and thin
+// inline-PTX wrappers for mbarrier, TMA and tcgen05 (sm_100-family).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Device status word bits (mirrored by the host's status codes).
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusNonFinite = 2u;
+
+// ------------------------------------------------------------------ bf16 --
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ------------------------------------------------------------------ E4M3 --
+// Non-negative block scale -> E4M3 code: round-to-nearest-even, saturating at
+// 448 (the hardware conversion with satfinite).  NaN is mapped to 0 by the
+// caller before this point.
+__device__ __forceinline__ uint32_t e4m3_encode(float t) {
+  return (uint32_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+}
+
+// E4M3 code -> fp32 (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ float e4m3_decode(uint32_t code) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// ------------------------------------------------------------------ E2M1 --
+// Two magnitudes (>= 0) -> one byte of E2M1 codes, round-to-nearest-even with
+// saturation at 6; a0 lands in the low nibble.  Feeding magnitudes keeps the
+// sign decision out of the conversion; the caller ORs the sign bits in.
+__device__ __forceinline__ uint32_t e2m1x2_rne_mag(float a0, float a1) {
+  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a0, a1), __NV_E2M1, cudaRoundNearest);
+}
+
+// Stochastic rounding of a magnitude a >= 0 with 16 random bits u.  With
+// lo <= a < hi adjacent E2M1 magnitudes the value rounds up iff
+// u * 2^-16 < (a - lo) / (hi - lo).  That fraction is read straight from the
+// fp32 bits:
+//   a in [1, 6):   a = 2^e (1 + f/2^23), lo = 2^e (1 + m1/2), gap 2^(e-1),
+//                  fraction = (f mod 2^22) / 2^22   -> up iff u * 64 < f22
+//   a in [0.5, 1): lo = 0.5, gap 0.5, fraction = f / 2^23 -> up iff u * 128 < f
+//   a in [0, 0.5): lo = 0, gap 0.5, fraction = 2a   -> up iff u * 2^-17 < a
+// Every comparison is exact, so the decision equals the real-number rule.
+__device__ __forceinline__ uint32_t e2m1_sr_mag(float a, uint32_t u) {
+  const uint32_t b = __float_as_uint(a);
+  const uint32_t e = (b >> 23) - 127u;
+  const uint32_t c_hi = 2u + 2u * e + ((b >> 22) & 1u) + (((u << 6) < (b & 0x3FFFFFu)) ? 1u : 0u);
+  const uint32_t c_mid = 1u + (((u << 7) < (b & 0x7FFFFFu)) ? 1u : 0u);
+  const uint32_t c_lo = (__uint2float_rn(u) * 0x1p-17f < a) ? 1u : 0u;
+  uint32_t c = (a >= 0.5f) ? c_mid : c_lo;
+  c = (a >= 1.0f) ? c_hi : c;
+  c = (a >= 6.0f) ? 7u : c;
+  return c;
+}
+
+__device__ __forceinline__ uint32_t sign_nibble(float v) { return (__float_as_uint(v) >> 31) << 3; }
+
+// ------------------------------------------------------------------ hash --
+// "lowbias32" 32-bit integer finaliser (C. Wellons, hash-prospector, 2018):
+// xorshift 16, *0x7feb352d, xorshift 15, *0x846ca68b, xorshift 16 (mod 2^32).
+__host__ __device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+// Key of a (64-bit seed, 32-bit stream tag) pair.
+__host__ __device__ __forceinline__ uint32_t stream_key(uint64_t seed, uint32_t tag) {
+  return mix32((uint32_t)seed ^ mix32((uint32_t)(seed >> 32) ^ tag));
+}
+
+constexpr uint32_t kTagSR = 0x5352u;   // stochastic-rounding stream
+constexpr uint32_t kTagRHT = 0x5248u;  // Hadamard sign stream
+
+// 16 random-sign bits of the transform's diagonal (bit j set: d_j = -1).
+__host__ __device__ __forceinline__ uint32_t rht_sign_bits(uint64_t rht_seed) {
+  return mix32(stream_key(rht_seed, kTagRHT)) & 0xFFFFu;
+}
+
+// Random bits for 16 consecutive output elements starting at index i0
+// (i0 % 16 == 0): one hash word per element pair; the even element takes
+// the low half-word.  hk = mix32(key ^ hi32(i0 >> 1)), shared by the pairs.
+__device__ __forceinline__ uint32_t sr_word(uint32_t hk, uint64_t pair_index) {
+  return mix32(hk ^ (uint32_t)pair_index);
+}
+
+// --------------------------------------------------------------- RHT-16 --
+// y = 1/4 * H16 * (d (.) x): sign flips, Walsh-Hadamard butterflies with
+// strides 1, 2, 4, 8 ((a, b) -> (a + b, a - b)), then the exact 1/4 scaling.
+// Same operation order as the definition, so results are bit-reproducible.
+__device__ __forceinline__ void rht16(float (&v)[16], uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = ((signs >> j) & 1u) ? -v[j] : v[j];
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+// ---------------------------------------------------------- block encode --
+// Scale of one block from its amax: sc = E4M3(amax_b / (s_g * 6)) or 0.
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float den) {
+  if (den == 0.0f) return 0u;
+  const float t = __fdiv_rn(amax_b, den);
+  return (t != t) ? 0u : e4m3_encode(t);
+}
+
+// Encoding factor 1 / (s_g * decode(sc)), 0 when the scale is 0.
+__device__ __forceinline__ float block_enc(float sg, uint32_t sc) {
+  const float scf = e4m3_decode(sc);
+  return (scf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sg, scf));
+}
+
+// Encode 16 values with a common factor into 8 bytes (two 32-bit words),
+// round-to-nearest-even.
+__device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    uint32_t byte = e2m1x2_rne_mag(fabsf(s0), fabsf(s1));
+    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
+    w[j / 8] |= byte << (8 * ((j / 2) % 4));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// Same with stochastic rounding: hk is the per-block hash key, q0 the pair
+// index of element 0 (8 pairs, one hash word each).
+__device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, uint32_t hk,
+                                             uint64_t q0) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
+    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    uint32_t byte = e2m1_sr_mag(fabsf(s0), r & 0xFFFFu) | (e2m1_sr_mag(fabsf(s1), r >> 16) << 4);
+    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
+    w[j / 8] |= byte << (8 * ((j / 2) % 4));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// Offset of scale (row r, block kb) in the MMA layout (cols/64 atoms per
+// 128-row band, 512 bytes per atom).
+__host__ __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t atoms_per_band) {
+  return ((r >> 7) * atoms_per_band + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+// --------------------------------------------------------------- PTX ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and raises the timeout
+// bit in *status) if the phase did not complete within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 1023u) == 0u && globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D TMA tile load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05 async operations
+// of this thread (MMAs, copies) have completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Copy a 32-row x 16-byte block of shared memory into tensor memory,
+// replicated into all four 32-lane sub-partitions.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D (+)= (A * SFA) x (B * SFB)^T, NVFP4 operands from shared memory, E4M3
+// scales from tensor memory, fp32 accumulator in tensor memory.
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive fp32 columns: thread i receives lane (base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,383 @@
+// nvfp4_gemm.cu -- block-scaled NVFP4 GEMM on the sm_103a tensor cores.
+//
+// C[M, N] = s_gA * s_gB * A[M, K] * B[N, K]^T, BF16 out.  The operands are
+// NVFP4 (E2M1 codes, one E4M3 scale per 16 elements along K): "NVFP4: cos'è e
+// come supera FP8 e BF16 nell'intelligenza artificiale", sections "Cos'è
+// NVFP4 ..." (format) and "Blackwell Architecture: la potenza dietro NVFP4"
+// (fifth-generation tensor cores scale NVFP4 blocks in hardware and keep
+// results in tensor memory next to the units).  All three MLP GEMMs of the
+// training recipe (fprop, dgrad, wgrad) take NVFP4 operands and return BF16:
+// readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: per 256-wide K step, the A tile (128 rows x
+//               128 B) and B tile (256 rows x 128 B) with 128-byte swizzle,
+//               plus the matching scale atoms (contiguous 512-byte blocks in
+//               the MMA scale layout) by bulk copy; 4-stage mbarrier ring.
+//   warp 1      MMA issuer: tcgen05.cp moves each stage's scales from shared
+//               to tensor memory (32x128b, replicated over the 4 lane
+//               quadrants), then four tcgen05.mma kind::mxf4nvf4
+//               block_scale.scale_vec::4X (M=128, N=256, K=64) accumulate
+//               into a 128 x 256 fp32 tile in tensor memory; tcgen05.commit
+//               frees the stage and, after the last K step, hands the tile to
+//               the epilogue.
+//   warps 2-9   epilogue: two warps per lane quadrant each pull 128 fp32
+//               columns into registers with tcgen05.ld, release the
+//               accumulator at once (the next tile's MMAs start while they
+//               write), scale by s_gA * s_gB, round to BF16 and store.
+// Tensor memory: 512 columns = accumulator [0, 256) + per-stage scale
+// columns (SFA 4 x 4, SFB 4 x 8 per stage).  Every mbarrier wait is bounded
+// (2 s); on expiry the kernel raises the timeout bit and winds down.
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+#include <mutex>
+
+namespace nvfp4 {
+namespace gemm {
+
+constexpr int BM = 128;            // tile rows (A rows)
+constexpr int BN = 256;            // tile cols (B rows)
+constexpr int BK = 256;            // K elements per stage
+constexpr int BKB = BK / 2;        // bytes per row per stage (128: one swizzle row)
+constexpr int MMA_K = 64;          // K per tcgen05.mma for kind::mxf4nvf4
+constexpr int KSTEPS = BK / MMA_K; // 4 MMAs per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BKB;                     // 16 KiB
+constexpr int B_BYTES = BN * BKB;                     // 32 KiB
+constexpr int SFA_BYTES = (BM / 128) * KSTEPS * 512;  // 2 KiB
+constexpr int SFB_BYTES = (BN / 128) * KSTEPS * 512;  // 4 KiB
+constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int NUM_THREADS = 320;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int TMEM_COLS = 512;
+constexpr int SF_COLS_PER_STAGE = KSTEPS * 4 + KSTEPS * 8;  // 48
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 2;
+constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr int SMEM_USED = OFF_ABORT + 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(256 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "tensor memory budget");
+
+// Instruction descriptor for kind::mxf4nvf4 (dense, K-major A and B, E2M1
+// operands, UE4M3 scales, scale-factor ids 0):
+//   [7,10) A format = E2M1 (1), [10,13) B format = E2M1 (1),
+//   [17,23) N >> 3, [23] scale type UE4M3 = 0, [24,29) M >> 4.
+constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+constexpr uint32_t IDESC = make_idesc(BM, BN);
+
+// Shared-memory matrix descriptor: start address, leading/stride byte
+// offsets (in 16-byte units), descriptor version 1 (bit 46), swizzle mode in
+// bits [61,64) (2 = 128-byte swizzle, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+
+// bf16 of acc * (hi + lo), rounded to nearest even as if the product were
+// exact: p = acc * hi is rounded once, e = acc * hi - p is recovered exactly
+// by an FMA, and r = e + acc * lo is the residual.  Since |r| is far below
+// half an fp32 ulp of p, p + r can only round differently from p when p sits
+// exactly on a bf16 tie, where the sign of r decides.
+__device__ __forceinline__ uint32_t scale_to_bf16(float acc, float hi, float lo) {
+  const float p = __fmul_rn(acc, hi);
+  const float e = __fmaf_rn(acc, hi, -p);
+  const float r = __fmaf_rn(acc, lo, e);
+  const uint32_t u = __float_as_uint(p);
+  const uint32_t rem = u & 0xFFFFu;
+  uint32_t up;
+  if (rem != 0x8000u) {
+    up = rem > 0x8000u ? 1u : 0u;
+  } else if (r == 0.0f) {
+    up = (u >> 16) & 1u;  // exact tie: to even
+  } else {
+    up = ((__float_as_uint(r) ^ u) >> 31) == 0u ? 1u : 0u;  // r pushes |p| up or down
+  }
+  if ((u & 0x7F800000u) == 0x7F800000u) up = 0u;  // inf / NaN pass through
+  return ((u >> 16) + up) & 0xFFFFu;
+}
+
+struct Params {
+  const uint8_t* sfa;  // A scales, MMA layout
+  const uint8_t* sfb;  // B scales, MMA layout
+  const float* sga;
+  const float* sgb;
+  uint16_t* c;  // bf16 output
+  int64_t ldc;
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles;
+  uint32_t* status;
+};
+
+// Tile order: groups of 16 M-tiles, M fastest inside a group, so the tiles
+// in flight across the GPU share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& tm, int& tn) {
+  constexpr int G = 16;
+  const int group_span = G * p.tiles_n;
+  const int g = t / group_span;
+  const int first_m = g * G;
+  const int gm = min(G, p.tiles_m - first_m);
+  const int r = t - g * group_span;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + OFF_BAR;                // STAGES barriers
+  const uint32_t bar_empty = bar_full + STAGES * 8;         // STAGES barriers
+  const uint32_t bar_tmem_full = bar_empty + STAGES * 8;
+  const uint32_t bar_tmem_empty = bar_tmem_full + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_tmem_full, 1);
+    mbar_init(bar_tmem_empty, NUM_EPI_WARPS);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmap_a);
+    prefetch_tensormap(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + OFF_TMEM_SLOT, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = p.K / BK;
+  const int64_t atoms_per_band = p.K / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const int bands_b = (p.N + 127) / 128;
+      for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(p, t, tm, tn);
+        const bool second_band = (2 * tn + 1) < bands_b;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
+          const uint32_t full = bar_full + 8 * stage;
+          const uint32_t tx = STAGE_TX - (second_band ? 0 : SFB_BYTES / 2);
+          mbar_arrive_expect_tx(full, tx);
+          tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, tm * BM, full);
+          tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN, full);
+          const uint8_t* sa = p.sfa + ((int64_t)tm * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
+          bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, sa, SFA_BYTES, full);
+          const uint8_t* sb0 = p.sfb + ((int64_t)(2 * tn) * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
+          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SFB_BYTES / 2, full);
+          if (second_band)
+            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SFB_BYTES / 2, sb0 + atoms_per_band * 512,
+                      SFB_BYTES / 2, full);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Let in-flight copies land before the CTA can exit: wait (bounded)
+      // for the last loads of every stage to complete.
+      for (int s = 0; s < STAGES; ++s) {
+        // stages issued in the current lap have parity `phase`, the others
+        // belong to the previous lap; waiting on either is bounded.
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        mbar_wait(bar_full + 8 * s, par, p.status, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x, ++it) {
+        if (!mbar_wait(bar_tmem_empty, (uint32_t)(it & 1) ^ 1u, p.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, p.status)) { *abort_flag = 1; ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_col = tmem_base + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
+          const uint32_t sfa_s = sbase + OFF_SFA + stage * SFA_BYTES;
+          const uint32_t sfb_s = sbase + OFF_SFB + stage * SFB_BYTES;
+#pragma unroll
+          for (int j = 0; j < KSTEPS; ++j) {
+            // one 512-byte atom = 32 rows x 16 bytes, 8-row groups 128 B apart
+            tc_cp_32x128b_warpx4(sf_col + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j + 4, smem_desc(sfb_s + SFB_BYTES / 2 + 512 * j, 0, 128, 0));
+          }
+          const uint32_t a_s = sbase + OFF_A + stage * A_BYTES;
+          const uint32_t b_s = sbase + OFF_B + stage * B_BYTES;
+#pragma unroll
+          for (int j = 0; j < KSTEPS; ++j) {
+            // K-major, 128-byte swizzle: 8-row groups 1024 B apart; the K
+            // offset inside the swizzle row advances the start address.
+            const uint64_t ad = smem_desc(a_s + 32 * j, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_s + 32 * j, 16, 1024, 2);
+            tc_mma_nvf4(tmem_base, ad, bd, IDESC, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                        (kb > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(bar_tmem_full);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int quad = warp & 3;          // lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;   // which 128 accumulator columns
+    // alpha = s_gA * s_gB as an unevaluated sum hi + lo (lo exact by FMA)
+    const float sga = *p.sga, sgb = *p.sgb;
+    const float alpha_hi = __fmul_rn(sga, sgb);
+    const float alpha_lo = __fmaf_rn(sga, sgb, -alpha_hi);
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      if (!mbar_wait(bar_tmem_full, (uint32_t)(it & 1), p.status)) { *abort_flag = 1; break; }
+      if (*abort_flag) break;
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(p, t, tm, tn);
+      uint32_t acc[128];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
+      tmem_ld_32x32b_x32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+      tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+      tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&acc[64]));
+      tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&acc[96]));
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tmem_empty);
+      const int row = tm * BM + quad * 32 + lane;
+      const int col0 = tn * BN + half * 128;
+      if (row < p.M) {
+        uint16_t* out = p.c + (int64_t)row * p.ldc + col0;
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            w[q] = scale_to_bf16(__uint_as_float(acc[8 * ch + 2 * q]), alpha_hi, alpha_lo) |
+                   (scale_to_bf16(__uint_as_float(acc[8 * ch + 2 * q + 1]), alpha_hi, alpha_lo) << 16);
+          }
+          const int n = col0 + 8 * ch;
+          if (n + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(out + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (n + q < p.N) out[8 * ch + q] = (uint16_t)(w[q / 2] >> (16 * (q & 1)));
+          }
+        }
+      }
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gemm
+
+// ----------------------------------------------------------------- host --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Byte-granular 2-D map over packed codes [rows, K/2] with a box of
+// (128 bytes, box_rows) and 128-byte swizzle; out-of-range rows read as zero.
+static bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
+  const cuuint32_t box[2] = {(cuuint32_t)gemm::BKB, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c, int64_t ldc,
+                cudaStream_t stream) {
+  using namespace gemm;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) return NVFP4_ERR_CUDA;
+    if (!attr_set[dev.device]) {
+      if (cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+          cudaSuccess)
+        return NVFP4_ERR_CUDA;
+      attr_set[dev.device] = true;
+    }
+  }
+  CUtensorMap ta, tb;
+  if (!make_code_map(&ta, A.codes, A.rows, A.cols / 2, BM)) return NVFP4_ERR_CUDA;
+  if (!make_code_map(&tb, B.codes, B.rows, B.cols / 2, BN)) return NVFP4_ERR_CUDA;
+  Params p;
+  p.sfa = A.scales;
+  p.sfb = B.scales;
+  p.sga = A.global_scale;
+  p.sgb = B.global_scale;
+  p.c = static_cast<uint16_t*>(c);
+  p.ldc = ldc;
+  p.M = (int)A.rows;
+  p.N = (int)B.rows;
+  p.K = (int)A.cols;
+  p.tiles_m = (p.M + BM - 1) / BM;
+  p.tiles_n = (p.N + BN - 1) / BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.status = dev.status;
+  const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
+  nvfp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,39 @@
+// nvfp4_internal.h -- host-side interfaces between the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+// Per-device state owned by the API layer.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  uint32_t* status = nullptr;  // device address of the status word
+};
+
+// Current device's info (filled once per device); nullptr on failure.
+const DeviceInfo* device_info();
+
+// Quantiser entry used by both public quantise calls.  Arguments have been
+// validated by the caller.
+int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t flags, bool rht, uint64_t rht_seed, uint64_t sr_seed,
+                    const float* amax_in, const nvfp4_tensor& out, cudaStream_t stream);
+
+// GEMM entry (arguments validated by the caller).
+int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
+                int64_t ldc, cudaStream_t stream);
+
+// Codec diagnostics.
+int encode_e2m1_rne_launch(const float* v, int64_t n, uint8_t* out, cudaStream_t stream);
+int encode_e2m1_sr_launch(const float* v, const uint16_t* u, int64_t n, uint8_t* out,
+                          cudaStream_t stream);
+int encode_e4m3_launch(const float* t, int64_t n, uint8_t* out, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,520 @@
+// nvfp4_quantize.cu -- HBM-bound NVFP4 quantisers for sm_103a.
+//
+// Format (E2M1 elements, one E4M3 scale per 16 values, one FP32 tensor
+// scale): "NVFP4: cos'è e come supera FP8 e BF16 nell'intelligenza
+// artificiale", section "Cos'è NVFP4 ..."; "FP4" (chaitex.ru/fp4), section
+// "Математическая структура FP4".  Recipe options (2D weight blocks, random
+// Hadamard transform for wgrad operands, stochastic rounding for gradients):
+// readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph.
+//
+// Kernels
+//   amax_*        : one read of the input, per-thread max, warp-shuffle and
+//                   CTA reduction, one atomicMax per CTA into the fp32 amax.
+//   quant_rows_*  : row-wise blocks straight from registers; a warp reads
+//                   1 KiB of contiguous input per 16-element step (1D) and
+//                   writes 256 contiguous code bytes.
+//   quant_cols    : blocks along the input's rows (transposed output): a
+//                   64 x 256 input tile is staged in shared memory with
+//                   coalesced 16-byte loads, then each thread owns a column
+//                   pair and walks four 16-row chunks.
+// All arithmetic on values is single-rounded IEEE fp32 (no contraction), so
+// results are bit-reproducible.
+#include <float.h>
+
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+struct QuantParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;  // input shape and row stride (elements)
+  int64_t orows, ocols;    // output shape
+  uint8_t* codes;
+  uint8_t* scales;
+  const float* amax_src;  // amax to use (caller's amax_in, or the amax pass result)
+  float* amax_out;        // written once when amax came from the caller, else null
+  float* sg_out;
+  uint32_t* status;
+  uint32_t sr_key;
+  uint32_t rht_signs;
+};
+
+// ------------------------------------------------------------- helpers --
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// CTA-wide max of a non-negative fp32 bit pattern, then one atomicMax.
+__device__ __forceinline__ void cta_amax_commit(uint32_t m, float* out) {
+  __shared__ uint32_t red[32];
+  m = warp_max_u32(m);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0u;
+    m = warp_max_u32(m);
+    if (lane == 0 && m != 0u) atomicMax(reinterpret_cast<unsigned int*>(out), m);
+  }
+}
+
+// Max |bf16| over a packed pair, as a 15-bit magnitude pattern per half.
+__device__ __forceinline__ uint32_t absmax_pairs(uint32_t m, const uint4& u) {
+  m = __vmaxu2(m, u.x & 0x7FFF7FFFu);
+  m = __vmaxu2(m, u.y & 0x7FFF7FFFu);
+  m = __vmaxu2(m, u.z & 0x7FFF7FFFu);
+  m = __vmaxu2(m, u.w & 0x7FFF7FFFu);
+  return m;
+}
+
+__device__ __forceinline__ uint32_t pairs_to_f32_bits(uint32_t m) {
+  return max(m & 0xFFFFu, m >> 16) << 16;  // bf16 magnitude -> fp32 pattern
+}
+
+// Tensor scale and the first-CTA bookkeeping (s_g, amax copy, non-finite flag).
+__device__ __forceinline__ float tensor_scale(const QuantParams& p, float& amax) {
+  amax = *p.amax_src;
+  const float sg = __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.sg_out = sg;
+    if (p.amax_out) *p.amax_out = amax;
+    if (!(amax <= FLT_MAX)) atomicOr(p.status, kStatusNonFinite);
+  }
+  return sg;
+}
+
+// ----------------------------------------------------------------- amax --
+// Plain amax of a bf16 matrix (vpr 16-byte vectors per row, row stride ldv
+// vectors).  Magnitudes are compared as integers (exact for bf16).
+__global__ void __launch_bounds__(256) amax_plain_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                         int64_t vpr, int64_t ldv, float* out) {
+  uint32_t m = 0u;
+  if (vpr == ldv) {
+    const int64_t n = rows * vpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+      const uint4 a = ldg_nc(x + i), b = ldg_nc(x + i + stride);
+      const uint4 c = ldg_nc(x + i + 2 * stride), d = ldg_nc(x + i + 3 * stride);
+      m = absmax_pairs(absmax_pairs(absmax_pairs(absmax_pairs(m, a), b), c), d);
+    }
+    for (; i < n; i += stride) m = absmax_pairs(m, ldg_nc(x + i));
+  } else {
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
+      for (int64_t v = threadIdx.x; v < vpr; v += blockDim.x) m = absmax_pairs(m, ldg_nc(x + r * ldv + v));
+  }
+  cta_amax_commit(pairs_to_f32_bits(m), out);
+}
+
+// amax after the row-wise transform: every 16 consecutive elements of a row.
+__global__ void __launch_bounds__(256) amax_rht_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ld, uint32_t signs,
+                                                            float* out) {
+  uint32_t m = 0u;
+  const uint32_t nb = (uint32_t)(cols / 16);
+  const uint32_t total = (uint32_t)(rows * nb);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t r = i / nb, b = i - r * nb;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ld + (int64_t)b * 16);
+    float v[16];
+    unpack16(ldg_nc(src), ldg_nc(src + 1), v);
+    rht16(v, signs);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(fabsf(v[j])));
+  }
+  cta_amax_commit(m, out);
+}
+
+// amax after the column-wise transform: every 16 consecutive rows of a
+// column.  A thread owns 16 rows x 8 columns (one 16-byte vector per row).
+__global__ void __launch_bounds__(256) amax_rht_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ld, uint32_t signs,
+                                                            float* out) {
+  uint32_t m = 0u;
+  const uint32_t nv = (uint32_t)(cols / 8);
+  const uint32_t total = (uint32_t)((rows / 16) * nv);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t rc = i / nv, vc = i - rc * nv;
+    const uint16_t* base = x + (int64_t)rc * 16 * ld + (int64_t)vc * 8;
+    uint4 u[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) u[k] = ldg_nc(base + (int64_t)k * ld);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t w = (c < 2) ? u[k].x : (c < 4) ? u[k].y : (c < 6) ? u[k].z : u[k].w;
+        v[k] = (c & 1) ? bf16_hi(w) : bf16_lo(w);
+      }
+      rht16(v, signs);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) m = max(m, __float_as_uint(fabsf(v[k])));
+    }
+  }
+  cta_amax_commit(m, out);
+}
+
+// ------------------------------------------------------- row-wise, 1D --
+template <bool kSR, bool kRHT, bool kMMA>
+__device__ __forceinline__ void quant_block_1d(const QuantParams& p, uint32_t i, uint32_t nb,
+                                               const uint4& a, const uint4& b4, float sg, float den) {
+  float v[16];
+  unpack16(a, b4, v);
+  if (kRHT) rht16(v, p.rht_signs);
+  float amax_b = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
+  const uint32_t sc = block_scale_code(amax_b, den);
+  const float enc = block_enc(sg, sc);
+  uint2 q;
+  if (kSR) {
+    const uint64_t q0 = (uint64_t)i * 8u;  // element index 16 i, pair index 8 i
+    q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+  } else {
+    q = encode16_rne(v, enc);
+  }
+  *reinterpret_cast<uint2*>(p.codes + (int64_t)i * 8) = q;
+  const uint32_t r = i / nb, kb = i - r * nb;
+  const int64_t off = kMMA ? mma_scale_offset(r, kb, nb / 4) : (int64_t)i;
+  p.scales[off] = (uint8_t)sc;
+}
+
+// One thread per 16-element block, two blocks in flight per thread.  The
+// output [rows, cols/2] is contiguous, so block i's codes sit at byte 8 i and
+// its elements have output indices 16 i .. 16 i + 15.
+template <bool kSR, bool kRHT, bool kMMA>
+__global__ void __launch_bounds__(256) quant_rows_1d_kernel(QuantParams p) {
+  float amax;
+  const float sg = tensor_scale(p, amax);
+  const float den = __fmul_rn(sg, 6.0f);
+  const uint32_t nb = (uint32_t)(p.ocols / 16);
+  const uint32_t total = (uint32_t)(p.orows * nb);
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + stride < total; i += 2 * stride) {
+    const uint32_t j = i + stride;
+    const uint32_t ri = i / nb, rj = j / nb;
+    const uint4* si = reinterpret_cast<const uint4*>(p.x + (int64_t)ri * p.ld + (int64_t)(i - ri * nb) * 16);
+    const uint4* sj = reinterpret_cast<const uint4*>(p.x + (int64_t)rj * p.ld + (int64_t)(j - rj * nb) * 16);
+    const uint4 a0 = ldg_nc(si), a1 = ldg_nc(si + 1), b0 = ldg_nc(sj), b1 = ldg_nc(sj + 1);
+    quant_block_1d<kSR, kRHT, kMMA>(p, i, nb, a0, a1, sg, den);
+    quant_block_1d<kSR, kRHT, kMMA>(p, j, nb, b0, b1, sg, den);
+  }
+  if (i < total) {
+    const uint32_t ri = i / nb;
+    const uint4* si = reinterpret_cast<const uint4*>(p.x + (int64_t)ri * p.ld + (int64_t)(i - ri * nb) * 16);
+    quant_block_1d<kSR, kRHT, kMMA>(p, i, nb, ldg_nc(si), ldg_nc(si + 1), sg, den);
+  }
+}
+
+// ------------------------------------------------------- row-wise, 2D --
+// One thread per aligned 16x16 tile: 16 rows x 32 bytes held in registers,
+// integer amax over the tile (exact for bf16), one scale for the tile written
+// on each of its 16 rows.
+template <bool kSR, bool kMMA>
+__global__ void __launch_bounds__(128) quant_rows_2d_kernel(QuantParams p) {
+  float amax;
+  const float sg = tensor_scale(p, amax);
+  const float den = __fmul_rn(sg, 6.0f);
+  const uint32_t nb = (uint32_t)(p.ocols / 16);
+  const uint32_t total = (uint32_t)((p.orows / 16) * nb);
+  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+    const uint32_t tr = t / nb, kb = t - tr * nb;
+    const uint16_t* base = p.x + (int64_t)tr * 16 * p.ld + (int64_t)kb * 16;
+    uint4 u[16][2];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const uint4* s = reinterpret_cast<const uint4*>(base + (int64_t)r * p.ld);
+      u[r][0] = ldg_nc(s);
+      u[r][1] = ldg_nc(s + 1);
+    }
+    uint32_t m = 0u;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m = absmax_pairs(absmax_pairs(m, u[r][0]), u[r][1]);
+    const float amax_b = __uint_as_float(pairs_to_f32_bits(m));
+    const uint32_t sc = block_scale_code(amax_b, den);
+    const float enc = block_enc(sg, sc);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int64_t orow = (int64_t)tr * 16 + r;
+      float v[16];
+      unpack16(u[r][0], u[r][1], v);
+      uint2 q;
+      if (kSR) {
+        const uint64_t q0 = ((uint64_t)orow * (uint64_t)p.ocols + (uint64_t)kb * 16u) >> 1;
+        q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+      } else {
+        q = encode16_rne(v, enc);
+      }
+      *reinterpret_cast<uint2*>(p.codes + orow * (p.ocols / 2) + (int64_t)kb * 8) = q;
+      const int64_t off = kMMA ? mma_scale_offset(orow, kb, nb / 4) : orow * nb + kb;
+      p.scales[off] = (uint8_t)sc;
+    }
+  }
+}
+
+// ------------------------------------------------- column-wise (x^T) --
+constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
+constexpr int kColTileCols = 256;  // input columns per tile
+constexpr int kColThreads = 128;   // one thread per column pair
+
+// Output row c = input column c, output column r = input row r.  Blocks run
+// along the input's rows; with kTwoD the 16x16 tile amax is shared by the 8
+// threads (16 columns) of a tile via shuffles.
+template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
+__global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) {
+  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  float amax;
+  const float sg = tensor_scale(p, amax);
+  const float den = __fmul_rn(sg, 6.0f);
+  const int64_t R = p.rows, C = p.cols;
+  const int64_t tiles_r = (R + kColTileRows - 1) / kColTileRows;
+  const int64_t tiles_c = (C + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = tiles_r * tiles_c;
+  const int tid = threadIdx.x;
+  const int64_t kb_per_row = R / 16;  // output blocks per output row
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
+    // stage the tile: a warp moves one 512-byte input row segment per step
+#pragma unroll 4
+    for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
+      const int idx = k * kColThreads + tid;
+      const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (r0 + row < R && c0 + vec * 8 < C) val = ldg_nc(p.x + (r0 + row) * p.ld + c0 + vec * 8);
+      *reinterpret_cast<uint4*>(&tile[row][vec * 4]) = val;
+    }
+    __syncthreads();
+    const int64_t c = c0 + 2 * tid;  // this thread's two output rows: c, c + 1
+    const bool col_ok = c < C;
+#pragma unroll 1
+    for (int k = 0; k < kColTileRows / 16; ++k) {
+      const int64_t rb = r0 + 16 * k;  // first input row of the block
+      if (rb >= R) break;              // uniform across the CTA
+      float v0[16], v1[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t w = tile[16 * k + i][tid];
+        v0[i] = bf16_lo(w);
+        v1[i] = bf16_hi(w);
+      }
+      if (kRHT) {
+        rht16(v0, p.rht_signs);
+        rht16(v1, p.rht_signs);
+      }
+      float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        a0 = fmaxf(a0, fabsf(v0[i]));
+        a1 = fmaxf(a1, fabsf(v1[i]));
+      }
+      if (kTwoD) {
+        float a = fmaxf(a0, a1);
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+        a0 = a1 = a;
+      }
+      if (!col_ok) continue;
+      const uint32_t sc0 = block_scale_code(a0, den), sc1 = block_scale_code(a1, den);
+      const float e0 = block_enc(sg, sc0), e1 = block_enc(sg, sc1);
+      uint2 q0, q1;
+      if (kSR) {
+        const uint64_t p0 = ((uint64_t)c * (uint64_t)R + (uint64_t)rb) >> 1;
+        const uint64_t p1 = ((uint64_t)(c + 1) * (uint64_t)R + (uint64_t)rb) >> 1;
+        q0 = encode16_sr(v0, e0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
+        q1 = encode16_sr(v1, e1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
+      } else {
+        q0 = encode16_rne(v0, e0);
+        q1 = encode16_rne(v1, e1);
+      }
+      *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
+      *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
+      const int64_t kb = rb / 16;
+      if (kMMA) {
+        p.scales[mma_scale_offset(c, kb, kb_per_row / 4)] = (uint8_t)sc0;
+        p.scales[mma_scale_offset(c + 1, kb, kb_per_row / 4)] = (uint8_t)sc1;
+      } else {
+        p.scales[c * kb_per_row + kb] = (uint8_t)sc0;
+        p.scales[(c + 1) * kb_per_row + kb] = (uint8_t)sc1;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------- launch --
+static int grid_for(const DeviceInfo& dev, int64_t work_items, int threads, int per_sm) {
+  const int64_t need = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)dev.sm_count * per_sm;
+  return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+template <bool kSR, bool kRHT>
+static void launch_rows_1d(const QuantParams& p, bool mma, int grid, cudaStream_t s) {
+  if (mma)
+    quant_rows_1d_kernel<kSR, kRHT, true><<<grid, 256, 0, s>>>(p);
+  else
+    quant_rows_1d_kernel<kSR, kRHT, false><<<grid, 256, 0, s>>>(p);
+}
+
+template <bool kSR, bool kRHT, bool kTwoD>
+static void launch_cols(const QuantParams& p, bool mma, int grid, cudaStream_t s) {
+  if (mma)
+    quant_cols_kernel<kSR, kRHT, kTwoD, true><<<grid, kColThreads, 0, s>>>(p);
+  else
+    quant_cols_kernel<kSR, kRHT, kTwoD, false><<<grid, kColThreads, 0, s>>>(p);
+}
+
+int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t flags, bool rht, uint64_t rht_seed, uint64_t sr_seed, const float* amax_in,
+                    const nvfp4_tensor& out, cudaStream_t stream) {
+  const bool two_d = (flags & NVFP4_BLOCK_2D) != 0;
+  const bool sr = rht || (flags & NVFP4_ROUND_SR) != 0;
+  const bool tr = (flags & NVFP4_TRANSPOSE_OUT) != 0;
+  const bool mma = out.scale_layout == NVFP4_SCALES_MMA;
+  const uint32_t signs = rht_sign_bits(rht_seed);
+
+  QuantParams p;
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = cols;
+  p.ld = ld;
+  p.orows = out.rows;
+  p.ocols = out.cols;
+  p.codes = out.codes;
+  p.scales = out.scales;
+  p.sg_out = out.global_scale;
+  p.status = dev.status;
+  p.sr_key = stream_key(sr_seed, kTagSR);
+  p.rht_signs = signs;
+
+  // Padding rows of the MMA scale layout read as zero.
+  if (mma && (p.orows % 128) != 0) {
+    const int64_t band = (p.ocols / 64) * 512;
+    if (cudaMemsetAsync(out.scales + (p.orows / 128) * band, 0, band, stream) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
+
+  // Pass 1: tensor amax (unless supplied).
+  if (amax_in) {
+    p.amax_src = amax_in;
+    p.amax_out = out.amax;
+  } else {
+    p.amax_src = out.amax;
+    p.amax_out = nullptr;
+    if (cudaMemsetAsync(out.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (!rht) {
+      const int64_t vpr = cols / 8;
+      amax_plain_kernel<<<grid_for(dev, rows * vpr / 4, 256, 8), 256, 0, stream>>>(
+          reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out.amax);
+    } else if (tr) {
+      amax_rht_cols_kernel<<<grid_for(dev, (rows / 16) * (cols / 8), 256, 4), 256, 0, stream>>>(
+          p.x, rows, cols, ld, signs, out.amax);
+    } else {
+      amax_rht_rows_kernel<<<grid_for(dev, rows * (cols / 16), 256, 8), 256, 0, stream>>>(
+          p.x, rows, cols, ld, signs, out.amax);
+    }
+  }
+
+  // Pass 2: scales and codes.
+  if (!tr) {
+    if (two_d) {
+      const int grid = grid_for(dev, (rows / 16) * (cols / 16), 128, 8);
+      if (sr) {
+        if (mma) quant_rows_2d_kernel<true, true><<<grid, 128, 0, stream>>>(p);
+        else quant_rows_2d_kernel<true, false><<<grid, 128, 0, stream>>>(p);
+      } else {
+        if (mma) quant_rows_2d_kernel<false, true><<<grid, 128, 0, stream>>>(p);
+        else quant_rows_2d_kernel<false, false><<<grid, 128, 0, stream>>>(p);
+      }
+    } else {
+      const int grid = grid_for(dev, rows * (cols / 16) / 2, 256, 8);
+      if (sr && rht) launch_rows_1d<true, true>(p, mma, grid, stream);
+      else if (sr) launch_rows_1d<true, false>(p, mma, grid, stream);
+      else if (rht) launch_rows_1d<false, true>(p, mma, grid, stream);
+      else launch_rows_1d<false, false>(p, mma, grid, stream);
+    }
+  } else {
+    const int64_t tiles = ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
+    const int64_t cap = (int64_t)dev.sm_count * 6;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    if (two_d) {
+      if (sr) launch_cols<true, false, true>(p, mma, grid, stream);
+      else launch_cols<false, false, true>(p, mma, grid, stream);
+    } else if (rht) {
+      launch_cols<true, true, false>(p, mma, grid, stream);
+    } else if (sr) {
+      launch_cols<true, false, false>(p, mma, grid, stream);
+    } else {
+      launch_cols<false, false, false>(p, mma, grid, stream);
+    }
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// ----------------------------------------------------- codec diagnostics --
+__global__ void encode_e2m1_rne_kernel(const float* v, int64_t n, uint8_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float a = v[i];
+    out[i] = (uint8_t)((e2m1x2_rne_mag(fabsf(a), 0.0f) & 0xFu) | sign_nibble(a));
+  }
+}
+
+__global__ void encode_e2m1_sr_kernel(const float* v, const uint16_t* u, int64_t n, uint8_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float a = v[i];
+    out[i] = (uint8_t)(e2m1_sr_mag(fabsf(a), u[i]) | sign_nibble(a));
+  }
+}
+
+__global__ void encode_e4m3_kernel(const float* t, int64_t n, uint8_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float a = t[i];
+    out[i] = (uint8_t)((a != a) ? 0u : e4m3_encode(a));
+  }
+}
+
+static int diag_grid(int64_t n) {
+  const int64_t g = (n + 255) / 256;
+  return (int)(g < 1 ? 1 : (g > 65536 ? 65536 : g));
+}
+
+int encode_e2m1_rne_launch(const float* v, int64_t n, uint8_t* out, cudaStream_t stream) {
+  encode_e2m1_rne_kernel<<<diag_grid(n), 256, 0, stream>>>(v, n, out);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int encode_e2m1_sr_launch(const float* v, const uint16_t* u, int64_t n, uint8_t* out, cudaStream_t stream) {
+  encode_e2m1_sr_kernel<<<diag_grid(n), 256, 0, stream>>>(v, u, n, out);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int encode_e4m3_launch(const float* t, int64_t n, uint8_t* out, cudaStream_t stream) {
+  encode_e4m3_kernel<<<diag_grid(n), 256, 0, stream>>>(t, n, out);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function that include/nvfp4.h declares, and rejects bad arguments before it
+touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_block_scaled_27_b300 as nv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_27_b300 import _build
+    _build.build()
+    return nv.load_library()
+
+
+def test_header_declares_the_three_hot_path_calls():
+    decl = _declared_functions()
+    for name in ("nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_gemm"):
+        assert name in decl
+
+
+def test_library_exports_every_declared_symbol(lib):
+    decl = _declared_functions()
+    assert decl, "no declarations parsed"
+    for name in decl:
+        assert hasattr(lib, name), f"missing export {name}"
+    assert set(decl) == set(nv.EXPORTED)
+
+
+def test_scales_bytes(lib):
+    assert nv.scales_bytes(256, 256, nv.SCALES_CANONICAL) == 256 * 16
+    assert nv.scales_bytes(256, 256, nv.SCALES_MMA) == 256 * 16
+    assert nv.scales_bytes(130, 64, nv.SCALES_MMA) == 256 * 4      # rows padded to 128
+    assert nv.scales_bytes(130, 64, nv.SCALES_CANONICAL) == 130 * 4
+    assert nv.scales_bytes(16, 48, nv.SCALES_MMA) == 0             # cols % 64 != 0
+    assert nv.scales_bytes(16, 40, nv.SCALES_CANONICAL) == 0       # cols % 16 != 0
+    assert nv.scales_bytes(16, 64, 7) == 0
+
+
+def test_status_strings_and_version(lib):
+    for code in (nv.OK, nv.ERR_INVALID_ARG, nv.ERR_UNSUPPORTED, nv.ERR_CUDA, nv.ERR_TIMEOUT, nv.ERR_NONFINITE):
+        s = lib.nvfp4_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.nvfp4_status_string(12345).decode() == "unknown status"
+    assert lib.nvfp4_version() >= 100
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    # null output descriptor, unknown flags, bad shapes: refused before any
+    # device work
+    assert lib.nvfp4_quantize(None, 16, 16, 16, 0, 0, None, None, None) == nv.ERR_INVALID_ARG
+    t = nv.CTensor(1, 1, 1, 1, 16, 16, nv.SCALES_CANONICAL, 0)
+    assert lib.nvfp4_quantize(16, 16, 16, 16, 0x80, 0, None, ctypes.byref(t), None) == nv.ERR_INVALID_ARG
+    t_bad = nv.CTensor(1, 1, 1, 1, 16, 24, nv.SCALES_CANONICAL, 0)  # cols % 16 != 0
+    assert lib.nvfp4_quantize(16, 16, 24, 24, 0, 0, None, ctypes.byref(t_bad), None) == nv.ERR_INVALID_ARG
+    t_shape = nv.CTensor(1, 1, 1, 1, 32, 16, nv.SCALES_CANONICAL, 0)  # wrong output shape
+    assert lib.nvfp4_quantize(16, 16, 16, 16, 0, 0, None, ctypes.byref(t_shape), None) == nv.ERR_INVALID_ARG
+    # RHT with 2D blocks is not a mode
+    assert lib.nvfp4_quantize_rht_sr(16, 16, 16, 16, nv.BLOCK_2D, 0, 0, None, ctypes.byref(t), None) \
+        == nv.ERR_INVALID_ARG
+    # GEMM: canonical scales, K mismatch, K % 256
+    a = nv.CTensor(16, 16, 16, 16, 128, 256, nv.SCALES_CANONICAL, 0)
+    b = nv.CTensor(16, 16, 16, 16, 128, 256, nv.SCALES_MMA, 0)
+    assert lib.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 16, 128, None) == nv.ERR_INVALID_ARG
+    a2 = nv.CTensor(16, 16, 16, 16, 128, 512, nv.SCALES_MMA, 0)
+    assert lib.nvfp4_gemm(ctypes.byref(a2), ctypes.byref(b), 16, 128, None) == nv.ERR_INVALID_ARG
+    a3 = nv.CTensor(16, 16, 16, 16, 128, 192, nv.SCALES_MMA, 0)
+    b3 = nv.CTensor(16, 16, 16, 16, 128, 192, nv.SCALES_MMA, 0)
+    assert lib.nvfp4_gemm(ctypes.byref(a3), ctypes.byref(b3), 16, 128, None) == nv.ERR_INVALID_ARG
+    # ldc below N
+    assert lib.nvfp4_gemm(ctypes.byref(b), ctypes.byref(b), 16, 64, None) == nv.ERR_INVALID_ARG
+
+
+def test_compute_calls_refuse_cpu_tensors():
+    import torch
+    x = torch.zeros(16, 16, dtype=torch.bfloat16)
+    with pytest.raises(nv.Nvfp4Error):
+        nv.quantize(x, layout=nv.SCALES_CANONICAL)
