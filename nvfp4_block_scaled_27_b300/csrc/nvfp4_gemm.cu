@@ -14,17 +14,24 @@
 //               128 B) and B tile (256 rows x 128 B) with 128-byte swizzle,
 //               plus the matching scale atoms (contiguous 512-byte blocks in
 //               the MMA scale layout) by bulk copy; 4-stage mbarrier ring.
-//   warp 1      MMA issuer: tcgen05.cp moves each stage's scales from shared
-//               to tensor memory (32x128b, replicated over the 4 lane
-//               quadrants), then four tcgen05.mma kind::mxf4nvf4
-//               block_scale.scale_vec::4X (M=128, N=256, K=64) accumulate
-//               into a 128 x 256 fp32 tile in tensor memory; tcgen05.commit
+//   warp 1      MMA issuer: four tcgen05.mma kind::mxf4nvf4
+//               block_scale.scale_vec::4X (M=128, N=256, K=64) per stage into
+//               a 128 x 256 fp32 accumulator in tensor memory; tcgen05.commit
 //               frees the stage and, after the last K step, hands the tile to
 //               the epilogue.
-//   warps 2-9   epilogue: two warps per lane quadrant each pull 128 fp32
-//               columns into registers with tcgen05.ld, release the
-//               accumulator at once (the next tile's MMAs start while they
-//               write), scale by s_gA * s_gB, round to BF16 and store.
+//   warps 2-5   scale writers, one per 32-lane tensor-memory quadrant: each
+//               lane reads its 16-byte rows of the stage's scale atoms from
+//               shared memory and writes them with tcgen05.st into that
+//               stage's scale columns (each quadrant holds the full
+//               128-row / 256-column scale set the MMA reads).  Moving scales
+//               this way keeps them off the MMA's in-order pipe; copying them
+//               with tcgen05.cp (12 copies per stage) stretched every MMA by
+//               about half.
+//   warps 6-13  epilogue: two warps per lane quadrant each pull 128 fp32
+//               columns out of tensor memory in 32-column chunks, release the
+//               accumulator after the last chunk (the next tile's MMAs start
+//               while they write), scale by s_gA * s_gB, round to BF16 and
+//               store.
 // Tensor memory: 512 columns = accumulator [0, 256) + per-stage scale
 // columns (SFA 4 x 4, SFB 4 x 8 per stage).  Every mbarrier wait is bounded
 // (2 s); on expiry the kernel raises the timeout bit and winds down.
@@ -48,8 +55,11 @@ constexpr int B_BYTES = BN * BKB;                     // 32 KiB
 constexpr int SFA_BYTES = (BM / 128) * KSTEPS * 512;  // 2 KiB
 constexpr int SFB_BYTES = (BN / 128) * KSTEPS * 512;  // 4 KiB
 constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 448;
+constexpr int NUM_SF_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
+constexpr int FIRST_SF_WARP = 2;
+constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COLS_PER_STAGE = KSTEPS * 4 + KSTEPS * 8;  // 48
 
@@ -59,7 +69,7 @@ constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2;
+constexpr int NUM_BARS = 3 * STAGES + 2;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
@@ -140,7 +150,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + OFF_BAR;                // STAGES barriers
   const uint32_t bar_empty = bar_full + STAGES * 8;         // STAGES barriers
-  const uint32_t bar_tmem_full = bar_empty + STAGES * 8;
+  const uint32_t bar_sf = bar_empty + STAGES * 8;           // STAGES barriers
+  const uint32_t bar_tmem_full = bar_sf + STAGES * 8;
   const uint32_t bar_tmem_empty = bar_tmem_full + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -152,6 +163,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
     }
     mbar_init(bar_tmem_full, 1);
     mbar_init(bar_tmem_empty, NUM_EPI_WARPS);
@@ -218,18 +230,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, p.status)) { *abort_flag = 1; ok = false; break; }
+          if (!mbar_wait(bar_full + 8 * stage, phase, p.status) || !mbar_wait(bar_sf + 8 * stage, phase, p.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sf_col = tmem_base + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
-          const uint32_t sfa_s = sbase + OFF_SFA + stage * SFA_BYTES;
-          const uint32_t sfb_s = sbase + OFF_SFB + stage * SFB_BYTES;
-#pragma unroll
-          for (int j = 0; j < KSTEPS; ++j) {
-            // one 512-byte atom = 32 rows x 16 bytes, 8-row groups 128 B apart
-            tc_cp_32x128b_warpx4(sf_col + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_warpx4(sf_col + 16 + 8 * j + 4, smem_desc(sfb_s + SFB_BYTES / 2 + 512 * j, 0, 128, 0));
-          }
           const uint32_t a_s = sbase + OFF_A + stage * A_BYTES;
           const uint32_t b_s = sbase + OFF_B + stage * B_BYTES;
 #pragma unroll
@@ -248,10 +255,48 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         tc_commit(bar_tmem_full);
       }
     }
+  } else if (warp < FIRST_EPI_WARP) {
+    // ---------------------------------------------------- scale writers --
+    // Quadrant q (= warp % 4) lanes 32q + r.  Scale atom row r holds the four
+    // 32-bit scale words of rows r, 32 + r, 64 + r, 96 + r (one per column),
+    // which is exactly what tensor-memory lane 32q + r needs in the four
+    // columns of a 128-row group.
+    const int quad = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(bar_full + 8 * stage, phase, p.status)) { *abort_flag = 1; ok = false; break; }
+        const uint8_t* sfa_s = smem + OFF_SFA + stage * SFA_BYTES + lane * 16;
+        const uint8_t* sfb_s = smem + OFF_SFB + stage * SFB_BYTES + lane * 16;
+        uint32_t va[16], vb[32];
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa_s + 512 * j);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_s + 512 * j);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + SFB_BYTES / 2 + 512 * j);
+          va[4 * j + 0] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+          vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+          vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
+        }
+        const uint32_t col = tmem_base + lane_off + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
+        tmem_st_32x32b_x16(col, va);
+        tmem_st_32x32b_x16(col + 16, vb);
+        tmem_st_32x32b_x16(col + 32, vb + 16);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf + 8 * stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
   } else {
     // --------------------------------------------------------- epilogue --
-    const int quad = warp & 3;          // lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;   // which 128 accumulator columns
+    const int quad = warp & 3;                     // lane quadrant this warp may access
+    const int half = (warp - FIRST_EPI_WARP) >> 2;  // which 128 accumulator columns
     // alpha = s_gA * s_gB as an unevaluated sum hi + lo (lo exact by FMA)
     const float sga = *p.sga, sgb = *p.sgb;
     const float alpha_hi = __fmul_rn(sga, sgb);
@@ -263,35 +308,40 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       tc_fence_after();
       int tm, tn;
       tile_coords(p, t, tm, tn);
-      uint32_t acc[128];
+      // Drain this warp's 32 x 128 accumulator block in 32-column chunks:
+      // load, scale and round each chunk, release the accumulator right after
+      // the last load, then write the row segment (64 bytes per chunk).
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
-      tmem_ld_32x32b_x32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
-      tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
-      tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&acc[64]));
-      tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&acc[96]));
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tmem_empty);
       const int row = tm * BM + quad * 32 + lane;
       const int col0 = tn * BN + half * 128;
-      if (row < p.M) {
-        uint16_t* out = p.c + (int64_t)row * p.ldc + col0;
+      uint16_t* out = p.c + (int64_t)row * p.ldc + col0;
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          uint32_t w[4];
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + 32 * ch, v);
+        tc_wait_ld();
+        if (ch == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tmem_empty);
+        }
+        uint32_t w[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            w[q] = scale_to_bf16(__uint_as_float(acc[8 * ch + 2 * q]), alpha_hi, alpha_lo) |
-                   (scale_to_bf16(__uint_as_float(acc[8 * ch + 2 * q + 1]), alpha_hi, alpha_lo) << 16);
-          }
-          const int n = col0 + 8 * ch;
-          if (n + 8 <= p.N) {
-            *reinterpret_cast<uint4*>(out + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
+        for (int q = 0; q < 16; ++q)
+          w[q] = scale_to_bf16(__uint_as_float(v[2 * q]), alpha_hi, alpha_lo) |
+                 (scale_to_bf16(__uint_as_float(v[2 * q + 1]), alpha_hi, alpha_lo) << 16);
+        if (row < p.M) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (n + q < p.N) out[8 * ch + q] = (uint16_t)(w[q / 2] >> (16 * (q & 1)));
+          for (int g = 0; g < 4; ++g) {
+            const int n = col0 + 32 * ch + 8 * g;
+            if (n + 8 <= p.N) {
+              *reinterpret_cast<uint4*>(out + 32 * ch + 8 * g) =
+                  make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (n + e < p.N) out[32 * ch + 8 * g + e] = (uint16_t)(w[4 * g + e / 2] >> (16 * (e & 1)));
+            }
           }
         }
       }
