@@ -394,6 +394,80 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- kernel cases --
+def _parse_case(spec):
+    """`gemm:M,N,K` or `quant:MODE:ROWS,COLS` (MODE in 1d, 1d_sr, 2d, 2d_t,
+    rht_t, 1d_amax_in)."""
+    parts = spec.split(":")
+    if parts[0] == "gemm" and len(parts) == 2:
+        return ("gemm", None, tuple(int(v) for v in parts[1].split(",")))
+    if parts[0] == "quant" and len(parts) == 3:
+        return ("quant", parts[1], tuple(int(v) for v in parts[2].split(",")))
+    raise SystemExit(f"bad --case {spec!r}")
+
+
+def run_cases(args):
+    """Single-op timings (CUDA events on the launching stream, L2 flushed
+    between repetitions) for tuning and for small ncu captures.  Prints one
+    JSON line per case; these are not the step benchmark."""
+    import nvfp4_block_scaled_27_b300 as nv
+    from workloads import TensorSpec
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    nv.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    preps = []
+    for spec in args.case:
+        kind, mode, dims = _parse_case(spec)
+        if kind == "gemm":
+            M, N, K = dims
+            a = make_bf16(TensorSpec(M, K, 1.0, 0.001, 30.0, 0), device=dev)
+            b = make_bf16(TensorSpec(N, K, 0.02, 0.0, 1.0, 1), device=dev)
+            qa, qb = nv.quantize(a), nv.quantize(b, nv.BLOCK_2D)
+            del a, b
+            c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            fn = (lambda qa=qa, qb=qb, c=c: nv.nvfp4_gemm(qa, qb, c, stream))
+            preps.append((spec, fn, 2.0 * M * N * K, "TFLOP/s"))
+        else:
+            R, C = dims
+            x = make_bf16(TensorSpec(R, C, 1.0, 0.001, 100.0, 0), device=dev)
+            tr = mode in ("2d_t", "rht_t")
+            out = nv.empty_nvfp4(C if tr else R, R if tr else C, device=dev)
+            ain = None
+            if mode == "1d_amax_in":
+                ain = x.abs().max().float().reshape(1)
+            flags = {"1d": 0, "1d_sr": nv.ROUND_SR, "2d": nv.BLOCK_2D, "2d_t": nv.BLOCK_2D | nv.TRANSPOSE_OUT,
+                     "rht_t": nv.TRANSPOSE_OUT, "1d_amax_in": 0}[mode]
+            if mode == "rht_t":
+                fn = (lambda x=x, out=out, flags=flags: nv.nvfp4_quantize_rht_sr(x, flags, RHT_SEED, 1001, None, out,
+                                                                                 stream))
+            else:
+                fn = (lambda x=x, out=out, flags=flags, ain=ain: nv.nvfp4_quantize(x, flags, 1001, ain, out, stream))
+            preps.append((spec, fn, QUANT_BYTES_PER_ELEM * R * C, "GB/s"))
+    torch.cuda.synchronize()
+    for spec, fn, work, unit in preps:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+            times = []
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                times.append((e0, e1))
+        stream.synchronize()
+        nv.check_status(stream)
+        ms = sorted(a.elapsed_time(b) for a, b in times)
+        med = ms[len(ms) // 2]
+        scale = 1e12 if unit == "TFLOP/s" else 1e9
+        print(json.dumps({"case": spec, "ms_median": round(med, 4), "ms_min": round(ms[0], 4),
+                          unit: round(work / (med * 1e-3) / scale, 1), "reps": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,10 +476,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", action="append", default=[],
+                    help="time single ops instead of the step: gemm:M,N,K or quant:MODE:ROWS,COLS")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.case:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_cases(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

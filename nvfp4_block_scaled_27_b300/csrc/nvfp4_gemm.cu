@@ -28,13 +28,14 @@
 //               with tcgen05.cp (12 copies per stage) stretched every MMA by
 //               about half.
 //   warps 6-13  epilogue: two warps per lane quadrant each pull 128 fp32
-//               columns out of tensor memory in 32-column chunks, release the
-//               accumulator after the last chunk (the next tile's MMAs start
-//               while they write), scale by s_gA * s_gB, round to BF16 and
-//               store.
+//               columns out of tensor memory, scale by s_gA * s_gB and round
+//               to packed BF16 in registers, release the accumulator (the
+//               next tile's MMAs start) and only then store.
 // Tensor memory: 512 columns = accumulator [0, 256) + per-stage scale
 // columns (SFA 4 x 4, SFB 4 x 8 per stage).  Every mbarrier wait is bounded
 // (2 s); on expiry the kernel raises the timeout bit and winds down.
+#include <cuda_bf16.h>
+
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 
@@ -94,27 +95,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
 }
 
-// bf16 of acc * (hi + lo), rounded to nearest even as if the product were
-// exact: p = acc * hi is rounded once, e = acc * hi - p is recovered exactly
-// by an FMA, and r = e + acc * lo is the residual.  Since |r| is far below
-// half an fp32 ulp of p, p + r can only round differently from p when p sits
-// exactly on a bf16 tie, where the sign of r decides.
-__device__ __forceinline__ uint32_t scale_to_bf16(float acc, float hi, float lo) {
-  const float p = __fmul_rn(acc, hi);
-  const float e = __fmaf_rn(acc, hi, -p);
-  const float r = __fmaf_rn(acc, lo, e);
-  const uint32_t u = __float_as_uint(p);
-  const uint32_t rem = u & 0xFFFFu;
-  uint32_t up;
-  if (rem != 0x8000u) {
-    up = rem > 0x8000u ? 1u : 0u;
-  } else if (r == 0.0f) {
-    up = (u >> 16) & 1u;  // exact tie: to even
-  } else {
-    up = ((__float_as_uint(r) ^ u) >> 31) == 0u ? 1u : 0u;  // r pushes |p| up or down
-  }
-  if ((u & 0x7F800000u) == 0x7F800000u) up = 0u;  // inf / NaN pass through
-  return ((u >> 16) + up) & 0xFFFFu;
+// Two accumulator values scaled by alpha and rounded to BF16 (nearest even),
+// packed with `lo` in the low half-word.  The product is rounded to fp32
+// first; the result differs from rounding the exact product only when that
+// fp32 value sits exactly on a BF16 tie.
+__device__ __forceinline__ uint32_t scale_pack_bf16x2(float lo, float hi, float alpha) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lo, alpha), __fmul_rn(hi, alpha));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 struct Params {
@@ -297,10 +284,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     // --------------------------------------------------------- epilogue --
     const int quad = warp & 3;                     // lane quadrant this warp may access
     const int half = (warp - FIRST_EPI_WARP) >> 2;  // which 128 accumulator columns
-    // alpha = s_gA * s_gB as an unevaluated sum hi + lo (lo exact by FMA)
-    const float sga = *p.sga, sgb = *p.sgb;
-    const float alpha_hi = __fmul_rn(sga, sgb);
-    const float alpha_lo = __fmaf_rn(sga, sgb, -alpha_hi);
+    const float alpha = __fmul_rn(*p.sga, *p.sgb);
     int it = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
       if (!mbar_wait(bar_tmem_full, (uint32_t)(it & 1), p.status)) { *abort_flag = 1; break; }
@@ -308,42 +292,55 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       tc_fence_after();
       int tm, tn;
       tile_coords(p, t, tm, tn);
-      // Drain this warp's 32 x 128 accumulator block in 32-column chunks:
-      // load, scale and round each chunk, release the accumulator right after
-      // the last load, then write the row segment (64 bytes per chunk).
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
       const int row = tm * BM + quad * 32 + lane;
       const int col0 = tn * BN + half * 128;
       uint16_t* out = p.c + (int64_t)row * p.ldc + col0;
+      if (col0 + 128 <= p.N) {
+        // Pull this warp's 32 x 128 accumulator block out of tensor memory
+        // in 32-column chunks, scaling and rounding each into 16 packed
+        // bf16x2 words; release the accumulator as soon as the last chunk is
+        // in registers so the next tile's MMAs overlap the stores.
+        uint32_t w[64];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + 32 * ch, v);
-        tc_wait_ld();
-        if (ch == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tmem_empty);
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + 32 * ch, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            w[16 * ch + q] = scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          w[q] = scale_to_bf16(__uint_as_float(v[2 * q]), alpha_hi, alpha_lo) |
-                 (scale_to_bf16(__uint_as_float(v[2 * q + 1]), alpha_hi, alpha_lo) << 16);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tmem_empty);
         if (row < p.M) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int n = col0 + 32 * ch + 8 * g;
-            if (n + 8 <= p.N) {
-              *reinterpret_cast<uint4*>(out + 32 * ch + 8 * g) =
-                  make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-            } else {
+          for (int g = 0; g < 16; ++g)
+            *reinterpret_cast<uint4*>(out + 8 * g) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+        }
+      } else {
+        // Ragged right edge (N not a multiple of the tile): chunk by chunk
+        // with per-element bounds, releasing the accumulator at the end.
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + 32 * ch, v);
+          tc_wait_ld();
+          if (row < p.M) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (n + e < p.N) out[32 * ch + 8 * g + e] = (uint16_t)(w[4 * g + e / 2] >> (16 * (e & 1)));
+            for (int q = 0; q < 16; ++q) {
+              const int n = col0 + 32 * ch + 2 * q;
+              const uint32_t pk =
+                  scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
+              if (n < p.N) out[32 * ch + 2 * q] = (uint16_t)(pk & 0xFFFFu);
+              if (n + 1 < p.N) out[32 * ch + 2 * q + 1] = (uint16_t)(pk >> 16);
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tmem_empty);
       }
     }
   }
