@@ -9,31 +9,36 @@
 // training recipe (fprop, dgrad, wgrad) take NVFP4 operands and return BF16:
 // readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: per 256-wide K step, the A tile (128 rows x
-//               128 B) and B tile (256 rows x 128 B) with 128-byte swizzle,
-//               plus the matching scale atoms (contiguous 512-byte blocks in
-//               the MMA scale layout) by bulk copy; 4-stage mbarrier ring.
-//   warp 1      MMA issuer: four tcgen05.mma kind::mxf4nvf4
-//               block_scale.scale_vec::4X (M=128, N=256, K=64) per stage into
-//               a 128 x 256 fp32 accumulator in tensor memory; tcgen05.commit
-//               frees the stage and, after the last K step, hands the tile to
-//               the epilogue.
-//   warps 2-5   scale writers, one per 32-lane tensor-memory quadrant: each
-//               lane reads its 16-byte rows of the stage's scale atoms from
-//               shared memory and writes them with tcgen05.st into that
-//               stage's scale columns (each quadrant holds the full
-//               128-row / 256-column scale set the MMA reads).  Moving scales
-//               this way keeps them off the MMA's in-order pipe; copying them
-//               with tcgen05.cp (12 copies per stage) stretched every MMA by
-//               about half.
+// Design: clusters of two CTAs (one per SM) work as a pair on 256 x 256
+// output tiles, persistently.  CTA r of the pair owns output rows
+// [128 r, 128 r + 128) of the tile.  Per 256-wide K step each CTA loads 128
+// rows of A and 128 of the 256 rows of B (so each SM streams half the B bytes
+// a single-SM 128 x 256 tile would need), its own A scales and all of B's
+// scales.  Warp roles, in both CTAs:
+//   warp 0      TMA producer: A and B boxes (128 rows x 128 B, 128-byte
+//               swizzle) and the scale atoms (bulk copies) into a 5-stage
+//               ring; completes on the CTA's own `full` barrier.
+//   warp 1      allocates the pair's tensor memory.  In CTA 0 (the leader)
+//               lane 0 issues tcgen05.mma.cta_group::2 kind::mxf4nvf4
+//               block_scale.scale_vec::4X (M = 256, N = 256, K = 64), four per
+//               stage, into a 128 x 256 fp32 accumulator in each CTA's tensor
+//               memory; tcgen05.commit multicasts stage release (`empty`) and
+//               tile completion (`tmem_full`) to both CTAs.
+//   warps 2-5   scale writers, one per 32-lane tensor-memory quadrant: copy
+//               the stage's scale atoms from shared memory into that stage's
+//               scale columns with tcgen05.st (each quadrant holds the whole
+//               set the MMA reads), then arrive on the leader's `sf_done`.
+//               (tcgen05.cp of the same data stalls the MMA stream.)
 //   warps 6-13  epilogue: two warps per lane quadrant each pull 128 fp32
 //               columns out of tensor memory, scale by s_gA * s_gB and round
-//               to packed BF16 in registers, release the accumulator (the
-//               next tile's MMAs start) and only then store.
-// Tensor memory: 512 columns = accumulator [0, 256) + per-stage scale
-// columns (SFA 4 x 4, SFB 4 x 8 per stage).  Every mbarrier wait is bounded
-// (2 s); on expiry the kernel raises the timeout bit and winds down.
+//               to packed BF16 in registers, release the accumulator to the
+//               leader (the next tile's MMAs start), then write 32 x 32 BF16
+//               boxes through swizzled shared memory with TMA stores.
+// Tensor memory (512 columns, same addresses in both CTAs): accumulator
+// [0, 256) + per-stage scale columns (SFA 4 x 4, SFB 4 x 8).  Every mbarrier
+// wait is bounded (2 s); on expiry the kernel raises the timeout bit, winds
+// down, and the two CTAs still meet in a bounded exit handshake before the
+// tensor memory is freed.
 #include <cuda_bf16.h>
 
 #include "nvfp4_device.cuh"
@@ -44,18 +49,20 @@
 namespace nvfp4 {
 namespace gemm {
 
-constexpr int BM = 128;            // tile rows (A rows)
-constexpr int BN = 256;            // tile cols (B rows)
+constexpr int BM = 128;            // output rows per CTA (A rows)
+constexpr int BM_PAIR = 2 * BM;    // output rows per pair tile
+constexpr int BN = 256;            // output cols per pair tile (B rows)
+constexpr int BN_CTA = BN / 2;     // B rows loaded by each CTA
 constexpr int BK = 256;            // K elements per stage
 constexpr int BKB = BK / 2;        // bytes per row per stage (128: one swizzle row)
 constexpr int MMA_K = 64;          // K per tcgen05.mma for kind::mxf4nvf4
 constexpr int KSTEPS = BK / MMA_K; // 4 MMAs per stage
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BKB;                     // 16 KiB
-constexpr int B_BYTES = BN * BKB;                     // 32 KiB
-constexpr int SFA_BYTES = (BM / 128) * KSTEPS * 512;  // 2 KiB
-constexpr int SFB_BYTES = (BN / 128) * KSTEPS * 512;  // 4 KiB
-constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BM * BKB;          // 16 KiB
+constexpr int B_BYTES = BN_CTA * BKB;      // 16 KiB
+constexpr int SF_BAND_BYTES = KSTEPS * 512;  // one 128-row band, one stage: 2 KiB
+constexpr int SFA_BYTES = SF_BAND_BYTES;
+constexpr int SFB_BYTES = 2 * SF_BAND_BYTES;
 constexpr int NUM_THREADS = 448;
 constexpr int NUM_SF_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
@@ -63,19 +70,24 @@ constexpr int FIRST_SF_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COLS_PER_STAGE = KSTEPS * 4 + KSTEPS * 8;  // 48
+constexpr int EPI_BOX = 32;                                  // 32 x 32 BF16 store boxes
+constexpr int EPI_BUF_BYTES = EPI_BOX * EPI_BOX * 2;         // 2 KiB
+constexpr int TILE_GROUP = 8;                                // pair tiles along M per raster group
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr int NUM_BARS = 3 * STAGES + 2;
+constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
+constexpr int NUM_BARS = 3 * STAGES + 4;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_EPI % 1024 == 0, "store staging must keep the swizzle pattern aligned");
 static_assert(256 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "tensor memory budget");
 
 // Instruction descriptor for kind::mxf4nvf4 (dense, K-major A and B, E2M1
@@ -85,7 +97,7 @@ static_assert(256 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "tensor memory budg
 constexpr uint32_t make_idesc(int m, int n) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-constexpr uint32_t IDESC = make_idesc(BM, BN);
+constexpr uint32_t IDESC = make_idesc(BM_PAIR, BN);
 
 // Shared-memory matrix descriptor: start address, leading/stride byte
 // offsets (in 16-byte units), descriptor version 1 (bit 46), swizzle mode in
@@ -109,21 +121,19 @@ struct Params {
   const uint8_t* sfb;  // B scales, MMA layout
   const float* sga;
   const float* sgb;
-  uint16_t* c;  // bf16 output
-  int64_t ldc;
   int M, N, K;
+  int bands_a, bands_b;  // 128-row scale bands present in the scale buffers
   int tiles_m, tiles_n, num_tiles;
   uint32_t* status;
 };
 
-// Tile order: groups of 16 M-tiles, M fastest inside a group, so the tiles
-// in flight across the GPU share A and B panels in L2.
+// Pair-tile order: groups of TILE_GROUP tiles along M, M fastest inside a
+// group, so the tiles in flight across the GPU share A and B panels in L2.
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int& tm, int& tn) {
-  constexpr int G = 16;
-  const int group_span = G * p.tiles_n;
+  const int group_span = TILE_GROUP * p.tiles_n;
   const int g = t / group_span;
-  const int first_m = g * G;
-  const int gm = min(G, p.tiles_m - first_m);
+  const int first_m = g * TILE_GROUP;
+  const int gm = min(TILE_GROUP, p.tiles_m - first_m);
   const int r = t - g * group_span;
   tm = first_m + r % gm;
   tn = r / gm;
@@ -131,40 +141,49 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& tm, int
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tmap_c, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + OFF_BAR;                // STAGES barriers
-  const uint32_t bar_empty = bar_full + STAGES * 8;         // STAGES barriers
-  const uint32_t bar_sf = bar_empty + STAGES * 8;           // STAGES barriers
-  const uint32_t bar_tmem_full = bar_sf + STAGES * 8;
-  const uint32_t bar_tmem_empty = bar_tmem_full + 8;
+  const uint32_t bar_full = sbase + OFF_BAR;             // STAGES: own TMA + bulk copies landed
+  const uint32_t bar_empty = bar_full + STAGES * 8;      // STAGES: pair MMAs done with the stage
+  const uint32_t bar_sf = bar_empty + STAGES * 8;        // STAGES: scales in tensor memory (leader)
+  const uint32_t bar_tmem_full = bar_sf + STAGES * 8;    // accumulator ready for the epilogue
+  const uint32_t bar_tmem_empty = bar_tmem_full + 8;     // accumulator drained (leader)
+  const uint32_t bar_exit = bar_tmem_empty + 8;          // peer CTA finished
+  const uint32_t bar_mma_done = bar_exit + 8;            // every pair MMA issued has completed
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = (int)cluster_id_x();
+  const int num_pairs = (int)cluster_count_x();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
+      mbar_init(bar_sf + 8 * s, 2 * NUM_SF_WARPS);
     }
     mbar_init(bar_tmem_full, 1);
-    mbar_init(bar_tmem_empty, NUM_EPI_WARPS);
+    mbar_init(bar_tmem_empty, 2 * NUM_EPI_WARPS);
+    mbar_init(bar_exit, 1);
+    mbar_init(bar_mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
+    prefetch_tensormap(&tmap_c);
   }
   if (warp == 1) {
-    tmem_alloc(sbase + OFF_TMEM_SLOT, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers must be initialised before either signals the other.
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = p.K / BK;
@@ -175,49 +194,50 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      const int bands_b = (p.N + 127) / 128;
-      for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
         int tm, tn;
         tile_coords(p, t, tm, tn);
-        const bool second_band = (2 * tn + 1) < bands_b;
+        const int band_a = 2 * tm + (int)rank;
+        const bool a_ok = band_a < p.bands_a;
+        const bool b1_ok = 2 * tn + 1 < p.bands_b;
+        const uint32_t tx = A_BYTES + B_BYTES + (a_ok ? SFA_BYTES : 0) + SF_BAND_BYTES + (b1_ok ? SF_BAND_BYTES : 0);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
+          if (!mbar_wait_cluster(bar_empty + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
           const uint32_t full = bar_full + 8 * stage;
-          const uint32_t tx = STAGE_TX - (second_band ? 0 : SFB_BYTES / 2);
           mbar_arrive_expect_tx(full, tx);
-          tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, tm * BM, full);
-          tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN, full);
-          const uint8_t* sa = p.sfa + ((int64_t)tm * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
-          bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, sa, SFA_BYTES, full);
+          tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, band_a * BM, full);
+          tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN + (int)rank * BN_CTA, full);
+          if (a_ok)
+            bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
+                      p.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
           const uint8_t* sb0 = p.sfb + ((int64_t)(2 * tn) * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
-          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SFB_BYTES / 2, full);
-          if (second_band)
-            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SFB_BYTES / 2, sb0 + atoms_per_band * 512,
-                      SFB_BYTES / 2, full);
+          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SF_BAND_BYTES, full);
+          if (b1_ok)
+            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SF_BAND_BYTES, sb0 + atoms_per_band * 512, SF_BAND_BYTES,
+                      full);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       // Let in-flight copies land before the CTA can exit: wait (bounded)
-      // for the last loads of every stage to complete.
+      // for the last phase issued on every stage.
       for (int s = 0; s < STAGES; ++s) {
-        // stages issued in the current lap have parity `phase`, the others
-        // belong to the previous lap; waiting on either is bounded.
         const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
         mbar_wait(bar_full + 8 * s, par, p.status, 100000000ull);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // ------------------------------------------- MMA issuer (leader CTA) --
+    if (rank == 0 && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x, ++it) {
-        if (!mbar_wait(bar_tmem_empty, (uint32_t)(it & 1) ^ 1u, p.status)) { *abort_flag = 1; break; }
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs, ++it) {
+        if (!mbar_wait_cluster(bar_tmem_empty, (uint32_t)(it & 1) ^ 1u, p.status)) { *abort_flag = 1; break; }
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, p.status) || !mbar_wait(bar_sf + 8 * stage, phase, p.status)) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, p.status) ||
+              !mbar_wait_cluster(bar_sf + 8 * stage, phase, p.status)) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -232,15 +252,18 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             // offset inside the swizzle row advances the start address.
             const uint64_t ad = smem_desc(a_s + 32 * j, 16, 1024, 2);
             const uint64_t bd = smem_desc(b_s + 32 * j, 16, 1024, 2);
-            tc_mma_nvf4(tmem_base, ad, bd, IDESC, sf_col + 4 * j, sf_col + 16 + 8 * j,
-                        (kb > 0 || j > 0) ? 1u : 0u);
+            tc_mma_nvf4_pair(tmem_base, ad, bd, IDESC, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                             (kb > 0 || j > 0) ? 1u : 0u);
           }
-          tc_commit(bar_empty + 8 * stage);
+          tc_commit_pair(bar_empty + 8 * stage, 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(bar_tmem_full);
+        tc_commit_pair(bar_tmem_full, 0x3);
       }
+      // Also on the abort paths: tell both CTAs when the last MMA issued has
+      // finished reading their shared memory and writing their tensor memory.
+      tc_commit_pair(bar_mma_done, 0x3);
     }
   } else if (warp < FIRST_EPI_WARP) {
     // ---------------------------------------------------- scale writers --
@@ -250,9 +273,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     // columns of a 128-row group.
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t leader_sf = mapa_shared(bar_sf, 0);
     int stage = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
+    for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
+      int tm, tn;
+      tile_coords(p, t, tm, tn);
+      const bool a_ok = 2 * tm + (int)rank < p.bands_a;
+      const bool b1_ok = 2 * tn + 1 < p.bands_b;
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(bar_full + 8 * stage, phase, p.status)) { *abort_flag = 1; ok = false; break; }
@@ -261,9 +289,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t va[16], vb[32];
 #pragma unroll
         for (int j = 0; j < KSTEPS; ++j) {
-          const uint4 a = *reinterpret_cast<const uint4*>(sfa_s + 512 * j);
+          uint4 a = *reinterpret_cast<const uint4*>(sfa_s + 512 * j);
           const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_s + 512 * j);
-          const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + SFB_BYTES / 2 + 512 * j);
+          uint4 b1 = *reinterpret_cast<const uint4*>(sfb_s + SF_BAND_BYTES + 512 * j);
+          if (!a_ok) a = make_uint4(0u, 0u, 0u, 0u);    // rows past the operand: zero scales
+          if (!b1_ok) b1 = make_uint4(0u, 0u, 0u, 0u);
           va[4 * j + 0] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
           vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
           vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
@@ -275,7 +305,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sf + 8 * stage);
+        if (lane == 0) mbar_arrive_cluster(leader_sf + 8 * stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -285,73 +315,82 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     const int quad = warp & 3;                     // lane quadrant this warp may access
     const int half = (warp - FIRST_EPI_WARP) >> 2;  // which 128 accumulator columns
     const float alpha = __fmul_rn(*p.sga, *p.sgb);
+    const uint32_t leader_tmem_empty = mapa_shared(bar_tmem_empty, 0);
+    const uint32_t stage_buf = sbase + OFF_EPI + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * EPI_BUF_BYTES);
+    const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
+    // Lane = row of the 32 x 32 box; its four 16-byte pieces go to swizzled
+    // positions (64-byte swizzle: piece c of row r at c ^ ((r >> 1) & 3)).
+    const uint32_t row_off = (uint32_t)lane * 64u;
+    const uint32_t swz = (uint32_t)((lane >> 1) & 3);
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      if (!mbar_wait(bar_tmem_full, (uint32_t)(it & 1), p.status)) { *abort_flag = 1; break; }
+    for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+      if (!mbar_wait_cluster(bar_tmem_full, (uint32_t)(it & 1), p.status)) { *abort_flag = 1; break; }
       if (*abort_flag) break;
       tc_fence_after();
       int tm, tn;
       tile_coords(p, t, tm, tn);
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
-      const int row = tm * BM + quad * 32 + lane;
+      // Pull this warp's 32 x 128 accumulator block out of tensor memory in
+      // 32-column chunks, scaling and rounding each into 16 packed bf16x2
+      // words; release the accumulator as soon as the last chunk is in
+      // registers so the next tile's MMAs overlap the stores.
+      uint32_t w[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + 32 * ch, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          w[16 * ch + q] = scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+      const int row0 = tm * BM_PAIR + (int)rank * BM + quad * 32;
       const int col0 = tn * BN + half * 128;
-      uint16_t* out = p.c + (int64_t)row * p.ldc + col0;
-      if (col0 + 128 <= p.N) {
-        // Pull this warp's 32 x 128 accumulator block out of tensor memory
-        // in 32-column chunks, scaling and rounding each into 16 packed
-        // bf16x2 words; release the accumulator as soon as the last chunk is
-        // in registers so the next tile's MMAs overlap the stores.
-        uint32_t w[64];
+      if (row0 >= p.M) continue;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + 32 * ch, v);
-          tc_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 16; ++q)
-            w[16 * ch + q] = scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
+      for (int ch = 0; ch < 4; ++ch) {
+        if (col0 + EPI_BOX * ch >= p.N) break;
+        const uint32_t buf = stage_buf + (uint32_t)((ch & 1) * EPI_BUF_BYTES);
+        // the store that last used this buffer must have read it
+        if (lane == 0) {
+          if (ch == 0)
+            bulk_wait_group_read<0>();
+          else
+            bulk_wait_group_read<1>();
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tmem_empty);
-        if (row < p.M) {
 #pragma unroll
-          for (int g = 0; g < 16; ++g)
-            *reinterpret_cast<uint4*>(out + 8 * g) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-        }
-      } else {
-        // Ragged right edge (N not a multiple of the tile): chunk by chunk
-        // with per-element bounds, releasing the accumulator at the end.
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + 32 * ch, v);
-          tc_wait_ld();
-          if (row < p.M) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const int n = col0 + 32 * ch + 2 * q;
-              const uint32_t pk =
-                  scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
-              if (n < p.N) out[32 * ch + 2 * q] = (uint16_t)(pk & 0xFFFFu);
-              if (n + 1 < p.N) out[32 * ch + 2 * q + 1] = (uint16_t)(pk >> 16);
-            }
-          }
-        }
-        tc_fence_before();
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(buf + row_off + (((uint32_t)c ^ swz) << 4), w[16 * ch + 4 * c], w[16 * ch + 4 * c + 1],
+                       w[16 * ch + 4 * c + 2], w[16 * ch + 4 * c + 3]);
+        fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tmem_empty);
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, buf, col0 + EPI_BOX * ch, row0);
+          bulk_commit_group();
+        }
       }
     }
+    if (lane == 0) bulk_wait_group<0>();
   }
 
   // ----------------------------------------------------------- teardown --
+  // Neither CTA may leave while the leader's MMAs can still use its shared
+  // and tensor memory, or while the other CTA can still signal its barriers.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait_cluster(bar_mma_done, 0, p.status, 10000000000ull);
+    mbar_arrive_cluster(mapa_shared(bar_exit, rank ^ 1u));
+    mbar_wait_cluster(bar_exit, 0, p.status, 10000000000ull);
+  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -377,53 +416,99 @@ static EncodeTiledFn encode_tiled_fn() {
 }
 
 // Byte-granular 2-D map over packed codes [rows, K/2] with a box of
-// (128 bytes, box_rows) and 128-byte swizzle; out-of-range rows read as zero.
-static bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes, uint32_t box_rows) {
+// (128 bytes, 128 rows) and 128-byte swizzle; out-of-range rows read as zero.
+static bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
-  const cuuint32_t box[2] = {(cuuint32_t)gemm::BKB, box_rows};
+  const cuuint32_t box[2] = {(cuuint32_t)gemm::BKB, (cuuint32_t)gemm::BM};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over the BF16 output [M, N] (row stride ldc elements) with 32 x 32 boxes
+// and 64-byte swizzle; stores outside [M, N] are dropped by the hardware.
+static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldc) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)ldc * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)gemm::EPI_BOX, (cuuint32_t)gemm::EPI_BOX};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c, int64_t ldc,
                 cudaStream_t stream) {
   using namespace gemm;
   static std::mutex mu;
-  static bool attr_set[64] = {};
+  static int max_pairs[64] = {};
+  int pairs_cap = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev.device < 0 || dev.device >= 64) return NVFP4_ERR_CUDA;
-    if (!attr_set[dev.device]) {
+    if (max_pairs[dev.device] == 0) {
       if (cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
           cudaSuccess)
         return NVFP4_ERR_CUDA;
-      attr_set[dev.device] = true;
+      // How many CTA pairs fit on the device at once (a persistent grid must
+      // not exceed it, or the surplus pairs would wait for a second wave).
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel, &cfg) != cudaSuccess || n <= 0)
+        return NVFP4_ERR_CUDA;
+      max_pairs[dev.device] = n;
     }
+    pairs_cap = max_pairs[dev.device];
   }
-  CUtensorMap ta, tb;
-  if (!make_code_map(&ta, A.codes, A.rows, A.cols / 2, BM)) return NVFP4_ERR_CUDA;
-  if (!make_code_map(&tb, B.codes, B.rows, B.cols / 2, BN)) return NVFP4_ERR_CUDA;
+  CUtensorMap ta, tb, tc;
+  if (!make_code_map(&ta, A.codes, A.rows, A.cols / 2)) return NVFP4_ERR_CUDA;
+  if (!make_code_map(&tb, B.codes, B.rows, B.cols / 2)) return NVFP4_ERR_CUDA;
+  if (!make_out_map(&tc, c, A.rows, B.rows, ldc)) return NVFP4_ERR_CUDA;
   Params p;
   p.sfa = A.scales;
   p.sfb = B.scales;
   p.sga = A.global_scale;
   p.sgb = B.global_scale;
-  p.c = static_cast<uint16_t*>(c);
-  p.ldc = ldc;
   p.M = (int)A.rows;
   p.N = (int)B.rows;
   p.K = (int)A.cols;
-  p.tiles_m = (p.M + BM - 1) / BM;
+  p.bands_a = (p.M + BM - 1) / BM;
+  p.bands_b = (p.N + BM - 1) / BM;
+  p.tiles_m = (p.M + BM_PAIR - 1) / BM_PAIR;
   p.tiles_n = (p.N + BN - 1) / BN;
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.status = dev.status;
-  const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
-  nvfp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  const int pairs = p.num_tiles < pairs_cap ? p.num_tiles : pairs_cap;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, ta, tb, tc, p) != cudaSuccess) return NVFP4_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
