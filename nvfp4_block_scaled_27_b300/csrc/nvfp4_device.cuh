@@ -41,25 +41,24 @@ __device__ __forceinline__ uint32_t e2m1x2_rne_mag(float a0, float a1) {
   return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a0, a1), __NV_E2M1, cudaRoundNearest);
 }
 
-// Stochastic rounding of a magnitude a >= 0 with 16 random bits u.  With
-// lo <= a < hi adjacent E2M1 magnitudes the value rounds up iff
-// u * 2^-16 < (a - lo) / (hi - lo).  That fraction is read straight from the
-// fp32 bits:
-//   a in [1, 6):   a = 2^e (1 + f/2^23), lo = 2^e (1 + m1/2), gap 2^(e-1),
-//                  fraction = (f mod 2^22) / 2^22   -> up iff u * 64 < f22
-//   a in [0.5, 1): lo = 0.5, gap 0.5, fraction = f / 2^23 -> up iff u * 128 < f
-//   a in [0, 0.5): lo = 0, gap 0.5, fraction = 2a   -> up iff u * 2^-17 < a
-// Every comparison is exact, so the decision equals the real-number rule.
-__device__ __forceinline__ uint32_t e2m1_sr_mag(float a, uint32_t u) {
-  const uint32_t b = __float_as_uint(a);
-  const uint32_t e = (b >> 23) - 127u;
-  const uint32_t c_hi = 2u + 2u * e + ((b >> 22) & 1u) + (((u << 6) < (b & 0x3FFFFFu)) ? 1u : 0u);
-  const uint32_t c_mid = 1u + (((u << 7) < (b & 0x7FFFFFu)) ? 1u : 0u);
-  const uint32_t c_lo = (__uint2float_rn(u) * 0x1p-17f < a) ? 1u : 0u;
-  uint32_t c = (a >= 0.5f) ? c_mid : c_lo;
-  c = (a >= 1.0f) ? c_hi : c;
-  c = (a >= 6.0f) ? 7u : c;
-  return c;
+// Stochastic rounding of a magnitude a >= 0: the E2M1 code (0..7) given
+// u64 = u << 6 for 16 random bits u.  With lo <= a < hi adjacent E2M1
+// magnitudes the value rounds up iff u * 2^-16 < (a - lo) / (hi - lo).
+//
+// Scaled by 2^-126, every E2M1 magnitude below 8 lands on a multiple of 2^22
+// in the fp32 bit pattern b (0.5 -> 1 << 22, 1 -> 2 << 22, 1.5 -> 3 << 22,
+// 2 -> 4 << 22, 3 -> 5 << 22, 4 -> 6 << 22, 6 -> 7 << 22): below 2 the scaled
+// values are subnormal or in the first normal binade (uniform spacing
+// 2^-149, i.e. b = a * 2^23), above 2 the top mantissa bit is the E2M1 one.
+// So lo = b >> 22 and (a - lo) / (hi - lo) = (b mod 2^22) / 2^22, and the
+// rule is "round up iff (b mod 2^22) > u * 64", i.e. add 2^22 - 1 - 64 u and
+// keep the bits above 22.  The scaling is exact for a >= 1; below 1 it is
+// rounded UP (ceil(a * 2^23)), which leaves every comparison of a * 2^23
+// against an integer threshold unchanged, so the decision equals the exact
+// rule.  Codes above 7 (a >= 6, after rounding) saturate to 7.
+__device__ __forceinline__ uint32_t e2m1_sr_code(float a, uint32_t u64) {
+  const uint32_t b = __float_as_uint(__fmul_ru(a, 0x1p-126f));
+  return min((b + 0x3FFFFFu - u64) >> 22, 7u);
 }
 
 __device__ __forceinline__ uint32_t sign_nibble(float v) { return (__float_as_uint(v) >> 31) << 3; }
@@ -147,7 +146,8 @@ __device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
 }
 
 // Same with stochastic rounding: hk is the per-block hash key, q0 the pair
-// index of element 0 (8 pairs, one hash word each).
+// index of element 0 (8 pairs, one hash word each; the even element uses the
+// low half-word).
 __device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, uint32_t hk,
                                              uint64_t q0) {
   uint32_t w[2] = {0u, 0u};
@@ -155,11 +155,40 @@ __device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, ui
   for (int j = 0; j < 16; j += 2) {
     const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
     const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
-    uint32_t byte = e2m1_sr_mag(fabsf(s0), r & 0xFFFFu) | (e2m1_sr_mag(fabsf(s1), r >> 16) << 4);
-    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
-    w[j / 8] |= byte << (8 * ((j / 2) % 4));
+    const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
+    const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
+    w[j / 8] |= (c0 | (c1 << 4)) << (8 * ((j / 2) % 4));
   }
   return make_uint2(w[0], w[1]);
+}
+
+// 8 values -> one 32-bit word of codes (element 2j in the low nibble of
+// byte j), round-to-nearest-even.
+__device__ __forceinline__ uint32_t encode8_rne(const float (&v)[8], float enc) {
+  uint32_t w = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    uint32_t byte = e2m1x2_rne_mag(fabsf(s0), fabsf(s1));
+    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
+    w |= byte << (4 * j);
+  }
+  return w;
+}
+
+// 8 values with stochastic rounding; q0 is the pair index of element 0 and
+// hk = mix32(key ^ hi32(q0)) (the 4 pairs share hi32).
+__device__ __forceinline__ uint32_t encode8_sr(const float (&v)[8], float enc, uint32_t hk, uint64_t q0) {
+  uint32_t w = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
+    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
+    const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
+    w |= (c0 | (c1 << 4)) << (4 * j);
+  }
+  return w;
 }
 
 // Offset of scale (row r, block kb) in the MMA layout (cols/64 atoms per

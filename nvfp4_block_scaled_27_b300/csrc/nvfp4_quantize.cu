@@ -21,6 +21,9 @@
 // results are bit-reproducible.
 #include <float.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 
@@ -105,7 +108,9 @@ __device__ __forceinline__ float tensor_scale(const QuantParams& p, float& amax)
 
 // ----------------------------------------------------------------- amax --
 // Plain amax of a bf16 matrix (vpr 16-byte vectors per row, row stride ldv
-// vectors).  Magnitudes are compared as integers (exact for bf16).
+// vectors).  Magnitudes are compared as integers (exact for bf16).  Eight
+// 16-byte loads in flight per thread keep enough bytes outstanding per SM to
+// cover DRAM latency.
 __global__ void __launch_bounds__(256) amax_plain_kernel(const uint4* __restrict__ x, int64_t rows,
                                                          int64_t vpr, int64_t ldv, float* out) {
   uint32_t m = 0u;
@@ -113,10 +118,12 @@ __global__ void __launch_bounds__(256) amax_plain_kernel(const uint4* __restrict
     const int64_t n = rows * vpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n; i += 4 * stride) {
-      const uint4 a = ldg_nc(x + i), b = ldg_nc(x + i + stride);
-      const uint4 c = ldg_nc(x + i + 2 * stride), d = ldg_nc(x + i + 3 * stride);
-      m = absmax_pairs(absmax_pairs(absmax_pairs(absmax_pairs(m, a), b), c), d);
+    for (; i + 7 * stride < n; i += 8 * stride) {
+      uint4 a[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = ldg_nc(x + i + k * stride);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = absmax_pairs(m, a[k]);
     }
     for (; i < n; i += stride) m = absmax_pairs(m, ldg_nc(x + i));
   } else {
@@ -229,47 +236,60 @@ __global__ void __launch_bounds__(256) quant_rows_1d_kernel(QuantParams p) {
 }
 
 // ------------------------------------------------------- row-wise, 2D --
-// One thread per aligned 16x16 tile: 16 rows x 32 bytes held in registers,
-// integer amax over the tile (exact for bf16), one scale for the tile written
-// on each of its 16 rows.
+// A warp owns a 16-row x 256-column strip (sixteen 16x16 tiles); lane l holds
+// columns [8 l, 8 l + 8) of all 16 rows (one 16-byte load per row, 512
+// contiguous bytes per warp load).  Lanes 2t and 2t + 1 share tile t: the
+// integer tile amax (exact for bf16) is combined with one shuffle, and the
+// tile's scale is written on each of its 16 rows.
 template <bool kSR, bool kMMA>
-__global__ void __launch_bounds__(128) quant_rows_2d_kernel(QuantParams p) {
+__global__ void __launch_bounds__(256) quant_rows_2d_kernel(QuantParams p) {
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
-  const uint32_t nb = (uint32_t)(p.ocols / 16);
-  const uint32_t total = (uint32_t)((p.orows / 16) * nb);
-  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
-    const uint32_t tr = t / nb, kb = t - tr * nb;
-    const uint16_t* base = p.x + (int64_t)tr * 16 * p.ld + (int64_t)kb * 16;
-    uint4 u[16][2];
+  const int lane = threadIdx.x & 31;
+  const uint32_t nb = (uint32_t)(p.ocols / 16);            // 16-column blocks per row
+  const uint32_t strips = (uint32_t)((p.ocols + 255) / 256);
+  const uint32_t total = (uint32_t)(p.orows / 16) * strips;  // warp work items
+  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += warps) {
+    const uint32_t band = w / strips, strip = w - band * strips;
+    const int64_t col = (int64_t)strip * 256 + 8 * lane;  // first of this lane's 8 columns
+    const bool active = col < p.ocols;                    // cols % 16 == 0: pairs are both in or out
+    const uint16_t* base = p.x + (int64_t)band * 16 * p.ld + col;
+    uint4 u[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const uint4* s = reinterpret_cast<const uint4*>(base + (int64_t)r * p.ld);
-      u[r][0] = ldg_nc(s);
-      u[r][1] = ldg_nc(s + 1);
-    }
+    for (int r = 0; r < 16; ++r) u[r] = active ? ldg_nc(base + (int64_t)r * p.ld) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t m = 0u;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) m = absmax_pairs(absmax_pairs(m, u[r][0]), u[r][1]);
-    const float amax_b = __uint_as_float(pairs_to_f32_bits(m));
-    const uint32_t sc = block_scale_code(amax_b, den);
+    for (int r = 0; r < 16; ++r) m = absmax_pairs(m, u[r]);
+    m = pairs_to_f32_bits(m);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    if (!active) continue;
+    const uint32_t sc = block_scale_code(__uint_as_float(m), den);
     const float enc = block_enc(sg, sc);
+    const uint32_t kb = (uint32_t)(col / 16);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      const int64_t orow = (int64_t)tr * 16 + r;
-      float v[16];
-      unpack16(u[r][0], u[r][1], v);
-      uint2 q;
-      if (kSR) {
-        const uint64_t q0 = ((uint64_t)orow * (uint64_t)p.ocols + (uint64_t)kb * 16u) >> 1;
-        q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
-      } else {
-        q = encode16_rne(v, enc);
+      const int64_t orow = (int64_t)band * 16 + r;
+      float v[8];
+      const uint32_t wd[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = bf16_lo(wd[i]);
+        v[2 * i + 1] = bf16_hi(wd[i]);
       }
-      *reinterpret_cast<uint2*>(p.codes + orow * (p.ocols / 2) + (int64_t)kb * 8) = q;
-      const int64_t off = kMMA ? mma_scale_offset(orow, kb, nb / 4) : orow * nb + kb;
-      p.scales[off] = (uint8_t)sc;
+      uint32_t q;
+      if (kSR) {
+        const uint64_t q0 = ((uint64_t)orow * (uint64_t)p.ocols + (uint64_t)col) >> 1;  // 4 pairs
+        q = encode8_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+      } else {
+        q = encode8_rne(v, enc);
+      }
+      *reinterpret_cast<uint32_t*>(p.codes + orow * (p.ocols / 2) + col / 2) = q;
+      if ((lane & 1) == 0) {
+        const int64_t off = kMMA ? mma_scale_offset(orow, kb, nb / 4) : orow * nb + kb;
+        p.scales[off] = (uint8_t)sc;
+      }
     }
   }
 }
@@ -366,26 +386,65 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) 
 }
 
 // ------------------------------------------------------------- launch --
-static int grid_for(const DeviceInfo& dev, int64_t work_items, int threads, int per_sm) {
+// CTAs that fit on the device at once for `kernel` (cached per kernel and
+// device).  Grid-stride kernels are launched with at most this many CTAs, so
+// every CTA is resident from the start and no partial second wave trails.
+static int64_t resident_ctas(const void* kernel, int threads, const DeviceInfo& dev) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> per_sm[64];
+  std::lock_guard<std::mutex> lock(mu);
+  auto& m = per_sm[dev.device & 63];
+  auto it = m.find(kernel);
+  if (it == m.end()) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    it = m.emplace(kernel, n).first;
+  }
+  return (int64_t)it->second * dev.sm_count;
+}
+
+template <typename Kernel>
+static int grid_for(Kernel kernel, const DeviceInfo& dev, int64_t work_items, int threads) {
   const int64_t need = (work_items + threads - 1) / threads;
-  const int64_t cap = (int64_t)dev.sm_count * per_sm;
+  const int64_t cap = resident_ctas(reinterpret_cast<const void*>(kernel), threads, dev);
   return (int)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
 template <bool kSR, bool kRHT>
-static void launch_rows_1d(const QuantParams& p, bool mma, int grid, cudaStream_t s) {
-  if (mma)
-    quant_rows_1d_kernel<kSR, kRHT, true><<<grid, 256, 0, s>>>(p);
-  else
-    quant_rows_1d_kernel<kSR, kRHT, false><<<grid, 256, 0, s>>>(p);
+static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+  const int64_t items = p.orows * (p.ocols / 16) / 2;  // two blocks per thread
+  if (mma) {
+    auto k = quant_rows_1d_kernel<kSR, kRHT, true>;
+    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+  } else {
+    auto k = quant_rows_1d_kernel<kSR, kRHT, false>;
+    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+  }
+}
+
+template <bool kSR>
+static void launch_rows_2d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+  const int64_t items = (p.orows / 16) * ((p.ocols + 255) / 256) * 32;  // one warp per strip
+  if (mma) {
+    auto k = quant_rows_2d_kernel<kSR, true>;
+    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+  } else {
+    auto k = quant_rows_2d_kernel<kSR, false>;
+    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+  }
 }
 
 template <bool kSR, bool kRHT, bool kTwoD>
-static void launch_cols(const QuantParams& p, bool mma, int grid, cudaStream_t s) {
-  if (mma)
-    quant_cols_kernel<kSR, kRHT, kTwoD, true><<<grid, kColThreads, 0, s>>>(p);
-  else
-    quant_cols_kernel<kSR, kRHT, kTwoD, false><<<grid, kColThreads, 0, s>>>(p);
+static void launch_cols(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+  const int64_t tiles =
+      ((p.rows + kColTileRows - 1) / kColTileRows) * ((p.cols + kColTileCols - 1) / kColTileCols);
+  if (mma) {
+    auto k = quant_cols_kernel<kSR, kRHT, kTwoD, true>;
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+  } else {
+    auto k = quant_cols_kernel<kSR, kRHT, kTwoD, false>;
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+  }
 }
 
 int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
@@ -428,13 +487,13 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
     if (cudaMemsetAsync(out.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (!rht) {
       const int64_t vpr = cols / 8;
-      amax_plain_kernel<<<grid_for(dev, rows * vpr / 4, 256, 8), 256, 0, stream>>>(
+      amax_plain_kernel<<<grid_for(amax_plain_kernel, dev, rows * vpr, 256), 256, 0, stream>>>(
           reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out.amax);
     } else if (tr) {
-      amax_rht_cols_kernel<<<grid_for(dev, (rows / 16) * (cols / 8), 256, 4), 256, 0, stream>>>(
+      amax_rht_cols_kernel<<<grid_for(amax_rht_cols_kernel, dev, (rows / 16) * (cols / 8), 256), 256, 0, stream>>>(
           p.x, rows, cols, ld, signs, out.amax);
     } else {
-      amax_rht_rows_kernel<<<grid_for(dev, rows * (cols / 16), 256, 8), 256, 0, stream>>>(
+      amax_rht_rows_kernel<<<grid_for(amax_rht_rows_kernel, dev, rows * (cols / 16), 256), 256, 0, stream>>>(
           p.x, rows, cols, ld, signs, out.amax);
     }
   }
@@ -442,34 +501,24 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
   // Pass 2: scales and codes.
   if (!tr) {
     if (two_d) {
-      const int grid = grid_for(dev, (rows / 16) * (cols / 16), 128, 8);
-      if (sr) {
-        if (mma) quant_rows_2d_kernel<true, true><<<grid, 128, 0, stream>>>(p);
-        else quant_rows_2d_kernel<true, false><<<grid, 128, 0, stream>>>(p);
-      } else {
-        if (mma) quant_rows_2d_kernel<false, true><<<grid, 128, 0, stream>>>(p);
-        else quant_rows_2d_kernel<false, false><<<grid, 128, 0, stream>>>(p);
-      }
+      if (sr) launch_rows_2d<true>(dev, p, mma, stream);
+      else launch_rows_2d<false>(dev, p, mma, stream);
     } else {
-      const int grid = grid_for(dev, rows * (cols / 16) / 2, 256, 8);
-      if (sr && rht) launch_rows_1d<true, true>(p, mma, grid, stream);
-      else if (sr) launch_rows_1d<true, false>(p, mma, grid, stream);
-      else if (rht) launch_rows_1d<false, true>(p, mma, grid, stream);
-      else launch_rows_1d<false, false>(p, mma, grid, stream);
+      if (sr && rht) launch_rows_1d<true, true>(dev, p, mma, stream);
+      else if (sr) launch_rows_1d<true, false>(dev, p, mma, stream);
+      else if (rht) launch_rows_1d<false, true>(dev, p, mma, stream);
+      else launch_rows_1d<false, false>(dev, p, mma, stream);
     }
   } else {
-    const int64_t tiles = ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
-    const int64_t cap = (int64_t)dev.sm_count * 6;
-    const int grid = (int)(tiles < cap ? tiles : cap);
     if (two_d) {
-      if (sr) launch_cols<true, false, true>(p, mma, grid, stream);
-      else launch_cols<false, false, true>(p, mma, grid, stream);
+      if (sr) launch_cols<true, false, true>(dev, p, mma, stream);
+      else launch_cols<false, false, true>(dev, p, mma, stream);
     } else if (rht) {
-      launch_cols<true, true, false>(p, mma, grid, stream);
+      launch_cols<true, true, false>(dev, p, mma, stream);
     } else if (sr) {
-      launch_cols<true, false, false>(p, mma, grid, stream);
+      launch_cols<true, false, false>(dev, p, mma, stream);
     } else {
-      launch_cols<false, false, false>(p, mma, grid, stream);
+      launch_cols<false, false, false>(dev, p, mma, stream);
     }
   }
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
@@ -486,7 +535,7 @@ __global__ void encode_e2m1_rne_kernel(const float* v, int64_t n, uint8_t* out) 
 __global__ void encode_e2m1_sr_kernel(const float* v, const uint16_t* u, int64_t n, uint8_t* out) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const float a = v[i];
-    out[i] = (uint8_t)(e2m1_sr_mag(fabsf(a), u[i]) | sign_nibble(a));
+    out[i] = (uint8_t)(e2m1_sr_code(fabsf(a), (uint32_t)u[i] << 6) | sign_nibble(a));
   }
 }
 

@@ -79,3 +79,47 @@ def test_e2m1_sr_boundaries_and_sample():
     bad = np.flatnonzero(got != exp)
     assert bad.size == 0, f"{bad.size} SR mismatches, first v={v[bad[0]]!r} u={u[bad[0]]} gpu {got[bad[0]]:#x} " \
                           f"oracle {exp[bad[0]]:#x}"
+
+
+def test_e2m1_sr_threshold_neighbours():
+    """Values a hair above, on, and below every SR decision threshold u*2^-16
+    of the fraction, in each E2M1 interval, including the sub-1 intervals
+    where a carries more fraction bits than the 2^-23 grid of the threshold
+    (a = (2^22 + 64 u + 1/2) / 2^23 and friends)."""
+    rng = np.random.default_rng(1)
+    us = np.unique(np.concatenate([[0, 1, 2, 3, 0x7FFF, 0x8000, 0xFFFE, 0xFFFF],
+                                   rng.integers(0, 65536, 200)])).astype(np.int64)
+    vals, uu = [], []
+    # intervals [lo, hi) with gap g: threshold value lo + g * u / 2^16
+    for lo, g in [(0.0, 0.5), (0.5, 0.5), (1.0, 0.5), (1.5, 0.5), (2.0, 1.0), (3.0, 1.0), (4.0, 2.0)]:
+        for u in us:
+            t = np.float64(lo) + np.float64(g) * u / 65536.0
+            for d in (-2, -1, 0, 1, 2):
+                # nudge by multiples of the float32 spacing at t (and at half of it below 1)
+                x = np.float32(t)
+                y = x
+                step = np.float32(np.inf) if d > 0 else np.float32(0)
+                for _ in range(abs(d)):
+                    y = np.nextafter(y, step)
+                if y >= 0:
+                    vals.append(y)
+                    uu.append(u)
+            # exact half-grid points below 1: (k + 1/2) * 2^-23
+            if lo < 1.0:
+                k = int(round(t * 2.0 ** 23))
+                for kk in (k - 1, k, k + 1):
+                    if kk >= 0:
+                        vals.append(np.float32((kk + 0.5) * 2.0 ** -23))
+                        uu.append(u)
+    v = np.array(vals, np.float32)
+    u = np.array(uu, np.uint16)
+    v = np.concatenate([v, -v])
+    u = np.concatenate([u, u])
+    out = torch.empty(v.size, dtype=torch.uint8, device="cuda")
+    nv.nvfp4_encode_e2m1_sr(torch.from_numpy(v).cuda(), torch.from_numpy(u.view(np.int16)).cuda(), out)
+    got = out.cpu().numpy()
+    exp = _oracle_sr(v, u)
+    bad = np.flatnonzero(got != exp)
+    assert bad.size == 0, f"{bad.size} of {v.size} SR mismatches, first v={v[bad[0]]!r} u={u[bad[0]]} " \
+                          f"gpu {got[bad[0]]:#x} oracle {exp[bad[0]]:#x}"
+
