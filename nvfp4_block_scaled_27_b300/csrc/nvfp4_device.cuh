@@ -249,6 +249,46 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return true;
 }
 
+// Bounded wait with the whole spin inside one asm block (no data-dependent
+// control flow in the caller's code): true once the phase with `parity` has
+// completed; after about limit_ns it raises the timeout bit and returns false.
+// Loops that issue tcgen05.mma keep their full rate only with this form.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, uint32_t* status,
+                                               uint64_t limit_ns = 2000000000ull) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1, P2;\n\t.reg .u64 t0, t1;\n\t.reg .u32 n;\n\t"
+      "mov.u64 t0, %%globaltimer;\n\tmov.u32 n, 0;\n"
+      "WAIT_%=:\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "@P1 bra.uni DONE_%=;\n\t"
+      "add.u32 n, n, 1;\n\t"
+      "and.b32 n, n, 1023;\n\t"
+      "setp.ne.u32 P2, n, 0;\n\t"
+      "@P2 bra.uni WAIT_%=;\n\t"
+      "mov.u64 t1, %%globaltimer;\n\t"
+      "sub.u64 t1, t1, t0;\n\t"
+      "setp.lt.u64 P2, t1, %3;\n\t"
+      "@P2 bra.uni WAIT_%=;\n\t"
+      "mov.u32 %0, 0;\n\t"
+      "bra.uni END_%=;\n"
+      "DONE_%=:\n\t"
+      "mov.u32 %0, 1;\n"
+      "END_%=:\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "l"(limit_ns)
+      : "memory");
+  if (!ok) atomicOr(status, kStatusTimeout);
+  return ok != 0;
+}
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

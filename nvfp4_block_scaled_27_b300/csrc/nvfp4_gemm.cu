@@ -227,43 +227,54 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------- MMA issuer (leader CTA) --
-    if (rank == 0 && lane == 0) {
+    // The whole warp runs the loop and waits (one bounded wait per stage, on
+    // the scale-done barrier, which both CTAs' scale writers reach only after
+    // their stage data has landed); one elected lane issues the MMAs.  A
+    // single-lane loop with two waits per stage measured ~40% slower.
+    if (rank == 0) {
+      const bool leader = elect_one();
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs, ++it) {
-        if (!mbar_wait_cluster(bar_tmem_empty, (uint32_t)(it & 1) ^ 1u, p.status)) { *abort_flag = 1; break; }
+      bool ok = true;
+      for (int t = pair; t < p.num_tiles && ok; t += num_pairs, ++it) {
+        // one vote keeps every lane's decision identical (waits and the
+        // abort flag are read per lane)
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait_spin(bar_tmem_empty, (uint32_t)(it & 1) ^ 1u, p.status) && !*abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, p.status) ||
-              !mbar_wait_cluster(bar_sf + 8 * stage, phase, p.status)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_sf + 8 * stage, phase, p.status));
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t sf_col = tmem_base + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
-          const uint32_t a_s = sbase + OFF_A + stage * A_BYTES;
-          const uint32_t b_s = sbase + OFF_B + stage * B_BYTES;
+          if (leader) {
+            const uint32_t sf_col = tmem_base + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
+            const uint32_t a_s = sbase + OFF_A + stage * A_BYTES;
+            const uint32_t b_s = sbase + OFF_B + stage * B_BYTES;
 #pragma unroll
-          for (int j = 0; j < KSTEPS; ++j) {
-            // K-major, 128-byte swizzle: 8-row groups 1024 B apart; the K
-            // offset inside the swizzle row advances the start address.
-            const uint64_t ad = smem_desc(a_s + 32 * j, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_s + 32 * j, 16, 1024, 2);
-            tc_mma_nvf4_pair(tmem_base, ad, bd, IDESC, sf_col + 4 * j, sf_col + 16 + 8 * j,
-                             (kb > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < KSTEPS; ++j) {
+              // K-major, 128-byte swizzle: 8-row groups 1024 B apart; the K
+              // offset inside the swizzle row advances the start address.
+              const uint64_t ad = smem_desc(a_s + 32 * j, 16, 1024, 2);
+              const uint64_t bd = smem_desc(b_s + 32 * j, 16, 1024, 2);
+              tc_mma_nvf4_pair(tmem_base, ad, bd, IDESC, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                               (kb > 0 || j > 0) ? 1u : 0u);
+            }
+            tc_commit_pair(bar_empty + 8 * stage, 0x3);
           }
-          tc_commit_pair(bar_empty + 8 * stage, 0x3);
+          __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit_pair(bar_tmem_full, 0x3);
+        if (leader) tc_commit_pair(bar_tmem_full, 0x3);
+        __syncwarp();
       }
+      if (!ok && leader) *abort_flag = 1;
       // Also on the abort paths: tell both CTAs when the last MMA issued has
       // finished reading their shared memory and writing their tensor memory.
-      tc_commit_pair(bar_mma_done, 0x3);
+      if (leader) tc_commit_pair(bar_mma_done, 0x3);
+      __syncwarp();
     }
   } else if (warp < FIRST_EPI_WARP) {
     // ---------------------------------------------------- scale writers --
