@@ -117,6 +117,58 @@ __device__ __forceinline__ void rht16(float (&v)[16], uint32_t signs) {
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
+// ---- packed fp32 pairs (each lane an IEEE round-to-nearest op, the same
+// result as the scalar instruction; two values per instruction) ----
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// The 16-point transform of two columns at once (lane 0: column a, lane 1:
+// column b), same operation order as rht16: sign flips, butterflies with
+// strides 1, 2, 4, 8, then the exact 1/4.
+__device__ __forceinline__ void rht16x2(float (&a)[16], float (&b)[16], uint32_t signs) {
+  uint64_t v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float d = ((signs >> j) & 1u) ? -1.0f : 1.0f;
+    v[j] = f2_mul(f2_pack(a[j], b[j]), f2_pack(d, d));
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const uint64_t x = v[i], y = v[i + h];
+        v[i] = f2_add(x, y);
+        v[i + h] = f2_sub(x, y);
+      }
+    }
+  }
+  const uint64_t q = f2_pack(0.25f, 0.25f);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) f2_unpack(f2_mul(v[j], q), a[j], b[j]);
+}
+
 // ---------------------------------------------------------- block encode --
 // Scale of one block from its amax: sc = E4M3(amax_b / (s_g * 6)) or 0.
 __device__ __forceinline__ uint32_t block_scale_code(float amax_b, float den) {
@@ -145,19 +197,78 @@ __device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
   return make_uint2(w[0], w[1]);
 }
 
+// Random words of the 8 pairs q0 .. q0 + 7 of a 16-element block (q0 a
+// multiple of 8): w_j = mix32(hk ^ lo32(q0 + j)), with hk = mix32(key ^
+// hi32(q0)).  Because j only touches the low 3 bits, the first xorshift is
+// shared (x ^ (x >> 16) = B ^ j with B = base ^ (base >> 16)) and the first
+// multiply splits into a shared part plus a 3-bit part.  Shifts right are
+// written as high products so most of the work runs on the multiply-add
+// pipe rather than the integer-logic pipe.
+__device__ __forceinline__ void sr_words8(uint32_t hk, uint32_t q0lo, uint32_t (&w)[8]) {
+  const uint32_t base = hk ^ q0lo;
+  const uint32_t b1 = base ^ __umulhi(base, 1u << 16);
+  const uint32_t hi = (b1 & ~7u) * 0x7feb352du;
+  const uint32_t lo3 = b1 & 7u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t x = hi + (lo3 ^ (uint32_t)j) * 0x7feb352du;
+    x ^= __umulhi(x, 1u << 17);  // x >> 15
+    x *= 0x846ca68bu;
+    x ^= __umulhi(x, 1u << 16);  // x >> 16
+    w[j] = x;
+  }
+}
+
+// SR codes (sign included, 4 bits each) of two values s0, s1 (already
+// scaled by the block's encoding factor) from one random word r: s0 uses the
+// low half-word, s1 the high half-word.  Returns c0 | c1 << 4.
+__device__ __forceinline__ uint32_t sr_pair_codes(float s0, float s1, uint32_t r) {
+  const uint32_t u_hi = __umulhi(r, 1u << 16);                      // r >> 16
+  const uint32_t n1 = 0x3FFFFFu - u_hi * 64u;                       // 2^22 - 1 - 64 u_odd
+  const uint32_t n0 = 0x3FFFFFu - r * 64u + u_hi * (1u << 22);      // 2^22 - 1 - 64 (r & 0xFFFF)
+  const uint32_t b0 = __float_as_uint(__fmul_ru(fabsf(s0), 0x1p-126f));
+  const uint32_t b1 = __float_as_uint(__fmul_ru(fabsf(s1), 0x1p-126f));
+  const uint32_t c0 = min(__umulhi(b0 + n0, 1u << 10), 7u);        // (b0 + n0) >> 22, saturated
+  const uint32_t c1 = min(__umulhi(b1 + n1, 1u << 10), 7u);
+  const uint32_t g0 = __umulhi(__float_as_uint(s0), 2u);            // sign bits
+  const uint32_t g1 = __umulhi(__float_as_uint(s1), 2u);
+  return c0 + c1 * 16u + g0 * 8u + g1 * 128u;
+}
+
+// SR codes of 16 values already multiplied by the block's encoding factor.
+__device__ __forceinline__ uint2 encode16_sr_scaled(const float (&sv)[16], uint32_t hk, uint64_t q0) {
+  uint32_t r[8];
+  sr_words8(hk, (uint32_t)q0, r);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) w[j / 8] += sr_pair_codes(sv[j], sv[j + 1], r[j / 2]) << (8 * ((j / 2) % 4));
+  return make_uint2(w[0], w[1]);
+}
+
+// RNE codes of 16 values already multiplied by the block's encoding factor.
+__device__ __forceinline__ uint2 encode16_rne_scaled(const float (&sv)[16]) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    uint32_t byte = e2m1x2_rne_mag(fabsf(sv[j]), fabsf(sv[j + 1]));
+    byte |= sign_nibble(sv[j]) | (sign_nibble(sv[j + 1]) << 4);
+    w[j / 8] |= byte << (8 * ((j / 2) % 4));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
 // Same with stochastic rounding: hk is the per-block hash key, q0 the pair
 // index of element 0 (8 pairs, one hash word each; the even element uses the
 // low half-word).
 __device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, uint32_t hk,
                                              uint64_t q0) {
+  uint32_t r[8];
+  sr_words8(hk, (uint32_t)q0, r);
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
-    const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
     const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
-    const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
-    const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
-    w[j / 8] |= (c0 | (c1 << 4)) << (8 * ((j / 2) % 4));
+    w[j / 8] += sr_pair_codes(s0, s1, r[j / 2]) << (8 * ((j / 2) % 4));
   }
   return make_uint2(w[0], w[1]);
 }
@@ -184,9 +295,7 @@ __device__ __forceinline__ uint32_t encode8_sr(const float (&v)[8], float enc, u
   for (int j = 0; j < 8; j += 2) {
     const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
     const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
-    const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
-    const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
-    w |= (c0 | (c1 << 4)) << (4 * j);
+    w += sr_pair_codes(s0, s1, r) << (4 * j);
   }
   return w;
 }

@@ -329,7 +329,14 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) 
     __syncthreads();
     const int64_t c = c0 + 2 * tid;  // this thread's two output rows: c, c + 1
     const bool col_ok = c < C;
-#pragma unroll 1
+    // Codes and scales of the tile's four 16-row chunks are collected and
+    // written together when the tile is whole: 32 contiguous code bytes per
+    // output row (two 16-byte stores) and one 32-bit word of four scales.
+    const bool whole = (r0 + kColTileRows <= R) && ((R & 31) == 0) &&
+                       ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0);
+    uint2 qa[4], qb[4];
+    uint32_t sca = 0u, scb = 0u;
+#pragma unroll
     for (int k = 0; k < kColTileRows / 16; ++k) {
       const int64_t rb = r0 + 16 * k;  // first input row of the block
       if (rb >= R) break;              // uniform across the CTA
@@ -340,10 +347,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) 
         v0[i] = bf16_lo(w);
         v1[i] = bf16_hi(w);
       }
-      if (kRHT) {
-        rht16(v0, p.rht_signs);
-        rht16(v1, p.rht_signs);
-      }
+      if (kRHT) rht16x2(v0, v1, p.rht_signs);
       float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -359,26 +363,55 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) 
       }
       if (!col_ok) continue;
       const uint32_t sc0 = block_scale_code(a0, den), sc1 = block_scale_code(a1, den);
-      const float e0 = block_enc(sg, sc0), e1 = block_enc(sg, sc1);
+      const uint64_t e01 = f2_pack(block_enc(sg, sc0), block_enc(sg, sc1));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f2_unpack(f2_mul(f2_pack(v0[i], v1[i]), e01), v0[i], v1[i]);
       uint2 q0, q1;
       if (kSR) {
         const uint64_t p0 = ((uint64_t)c * (uint64_t)R + (uint64_t)rb) >> 1;
         const uint64_t p1 = ((uint64_t)(c + 1) * (uint64_t)R + (uint64_t)rb) >> 1;
-        q0 = encode16_sr(v0, e0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
-        q1 = encode16_sr(v1, e1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
+        q0 = encode16_sr_scaled(v0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
+        q1 = encode16_sr_scaled(v1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
       } else {
-        q0 = encode16_rne(v0, e0);
-        q1 = encode16_rne(v1, e1);
+        q0 = encode16_rne_scaled(v0);
+        q1 = encode16_rne_scaled(v1);
       }
-      *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
-      *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
-      const int64_t kb = rb / 16;
+      qa[k] = q0;
+      qb[k] = q1;
+      sca |= sc0 << (8 * k);
+      scb |= sc1 << (8 * k);
+      if (!whole) {
+        *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
+        *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
+        const int64_t kb = rb / 16;
+        if (kMMA) {
+          p.scales[mma_scale_offset(c, kb, kb_per_row / 4)] = (uint8_t)sc0;
+          p.scales[mma_scale_offset(c + 1, kb, kb_per_row / 4)] = (uint8_t)sc1;
+        } else {
+          p.scales[c * kb_per_row + kb] = (uint8_t)sc0;
+          p.scales[(c + 1) * kb_per_row + kb] = (uint8_t)sc1;
+        }
+      }
+    }
+    if (whole && col_ok) {
+      uint8_t* o0 = p.codes + c * (R / 2) + r0 / 2;
+      uint8_t* o1 = o0 + R / 2;
+      *reinterpret_cast<uint4*>(o0) = make_uint4(qa[0].x, qa[0].y, qa[1].x, qa[1].y);
+      *reinterpret_cast<uint4*>(o0 + 16) = make_uint4(qa[2].x, qa[2].y, qa[3].x, qa[3].y);
+      *reinterpret_cast<uint4*>(o1) = make_uint4(qb[0].x, qb[0].y, qb[1].x, qb[1].y);
+      *reinterpret_cast<uint4*>(o1 + 16) = make_uint4(qb[2].x, qb[2].y, qb[3].x, qb[3].y);
+      const int64_t kb0 = r0 / 16;  // a multiple of 4: the four scales share one word
       if (kMMA) {
-        p.scales[mma_scale_offset(c, kb, kb_per_row / 4)] = (uint8_t)sc0;
-        p.scales[mma_scale_offset(c + 1, kb, kb_per_row / 4)] = (uint8_t)sc1;
+        *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c, kb0, kb_per_row / 4)) = sca;
+        *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c + 1, kb0, kb_per_row / 4)) = scb;
       } else {
-        p.scales[c * kb_per_row + kb] = (uint8_t)sc0;
-        p.scales[(c + 1) * kb_per_row + kb] = (uint8_t)sc1;
+        uint8_t* s0 = p.scales + c * kb_per_row + kb0;
+        uint8_t* s1 = s0 + kb_per_row;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s0[k] = (uint8_t)(sca >> (8 * k));
+          s1[k] = (uint8_t)(scb >> (8 * k));
+        }
       }
     }
     __syncthreads();
