@@ -15,30 +15,37 @@
 // rows of A and 128 of the 256 rows of B (so each SM streams half the B bytes
 // a single-SM 128 x 256 tile would need), its own A scales and all of B's
 // scales.  Warp roles, in both CTAs:
-//   warp 0      TMA producer: A and B boxes (128 rows x 128 B, 128-byte
-//               swizzle) and the scale atoms (bulk copies) into a 5-stage
-//               ring; completes on the CTA's own `full` barrier.
+//   warp 0      operand producer: A and B boxes (128 rows x 128 B, 128-byte
+//               swizzle) into a 5-stage ring; the copies of both CTAs
+//               complete on the leader's `full` barrier (CTA-pair TMA form).
 //   warp 1      allocates the pair's tensor memory.  In CTA 0 (the leader)
-//               lane 0 issues tcgen05.mma.cta_group::2 kind::mxf4nvf4
-//               block_scale.scale_vec::4X (M = 256, N = 256, K = 64), four per
-//               stage, into a 128 x 256 fp32 accumulator in each CTA's tensor
-//               memory; tcgen05.commit multicasts stage release (`empty`) and
-//               tile completion (`tmem_full`) to both CTAs.
-//   warps 2-5   scale writers, one per 32-lane tensor-memory quadrant: copy
-//               the stage's scale atoms from shared memory into that stage's
-//               scale columns with tcgen05.st (each quadrant holds the whole
-//               set the MMA reads), then arrive on the leader's `sf_done`.
-//               (tcgen05.cp of the same data stalls the MMA stream.)
-//   warps 6-13  epilogue: two warps per lane quadrant each pull 128 fp32
+//               the whole warp waits and one elected lane issues
+//               tcgen05.mma.cta_group::2 kind::mxf4nvf4 block_scale
+//               .scale_vec::4X (M = 256, N = 256, K = 64), four per stage,
+//               into a 128 x 256 fp32 accumulator in each CTA's tensor
+//               memory; tcgen05.commit multicasts stage release (`empty`)
+//               and tile completion (`tmem_full`) to both CTAs.
+//   warp 2      scale producer: the stage's scale atoms (bulk copies) into a
+//               ring of its own, refilled as soon as the scale writers have
+//               read a slot, so scales are in shared memory well before the
+//               stage's operands.
+//   warps 3-6   scale writers, one per 32-lane tensor-memory quadrant: once
+//               the stage's scale columns are free (its previous MMAs done),
+//               copy the scale atoms from shared memory into them with
+//               tcgen05.st (each quadrant holds the whole set the MMA reads)
+//               and arrive on the leader's `sf_done`.  (tcgen05.cp of the
+//               same data stalls the MMA stream.)
+//   warps 7-14  epilogue: two warps per lane quadrant each pull 128 fp32
 //               columns out of tensor memory, scale by s_gA * s_gB and round
 //               to packed BF16 in registers, release the accumulator to the
 //               leader (the next tile's MMAs start), then write 32 x 32 BF16
 //               boxes through swizzled shared memory with TMA stores.
-// Tensor memory (512 columns, same addresses in both CTAs): accumulator
-// [0, 256) + per-stage scale columns (SFA 4 x 4, SFB 4 x 8).  Every mbarrier
-// wait is bounded (2 s); on expiry the kernel raises the timeout bit, winds
-// down, and the two CTAs still meet in a bounded exit handshake before the
-// tensor memory is freed.
+// The refill of a stage thus waits only on the operand copies; scales are
+// written off that path.  Tensor memory (512 columns, same addresses in both
+// CTAs): accumulator [0, 256) + per-stage scale columns (SFA 4 x 4, SFB 4 x 8).
+// Every mbarrier wait is bounded (2 s); on expiry the kernel raises the
+// timeout bit, winds down, and the two CTAs still meet in a bounded exit
+// handshake before the tensor memory is freed.
 #include <cuda_bf16.h>
 
 #include "nvfp4_device.cuh"
@@ -63,10 +70,11 @@ constexpr int B_BYTES = BN_CTA * BKB;      // 16 KiB
 constexpr int SF_BAND_BYTES = KSTEPS * 512;  // one 128-row band, one stage: 2 KiB
 constexpr int SFA_BYTES = SF_BAND_BYTES;
 constexpr int SFB_BYTES = 2 * SF_BAND_BYTES;
-constexpr int NUM_THREADS = 448;
+constexpr int NUM_THREADS = 480;
 constexpr int NUM_SF_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int FIRST_SF_WARP = 2;
+constexpr int SF_PRODUCER_WARP = 2;
+constexpr int FIRST_SF_WARP = 3;
 constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COLS_PER_STAGE = KSTEPS * 4 + KSTEPS * 8;  // 48
@@ -81,7 +89,7 @@ constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
 constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
-constexpr int NUM_BARS = 3 * STAGES + 4;
+constexpr int NUM_BARS = 5 * STAGES + 4;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
@@ -145,10 +153,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + OFF_BAR;             // STAGES: own TMA + bulk copies landed
+  const uint32_t bar_full = sbase + OFF_BAR;             // STAGES: both CTAs' A/B landed (leader)
   const uint32_t bar_empty = bar_full + STAGES * 8;      // STAGES: pair MMAs done with the stage
   const uint32_t bar_sf = bar_empty + STAGES * 8;        // STAGES: scales in tensor memory (leader)
-  const uint32_t bar_tmem_full = bar_sf + STAGES * 8;    // accumulator ready for the epilogue
+  const uint32_t bar_sf_full = bar_sf + STAGES * 8;      // STAGES: scale atoms in shared memory
+  const uint32_t bar_sf_free = bar_sf_full + STAGES * 8; // STAGES: scale slot read by the writers
+  const uint32_t bar_tmem_full = bar_sf_free + STAGES * 8;  // accumulator ready for the epilogue
   const uint32_t bar_tmem_empty = bar_tmem_full + 8;     // accumulator drained (leader)
   const uint32_t bar_exit = bar_tmem_empty + 8;          // peer CTA finished
   const uint32_t bar_mma_done = bar_exit + 8;            // every pair MMA issued has completed
@@ -166,6 +176,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, 2 * NUM_SF_WARPS);
+      mbar_init(bar_sf_full + 8 * s, 1);
+      mbar_init(bar_sf_free + 8 * s, NUM_SF_WARPS);
     }
     mbar_init(bar_tmem_full, 1);
     mbar_init(bar_tmem_empty, 2 * NUM_EPI_WARPS);
@@ -190,47 +202,33 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   const int64_t atoms_per_band = p.K / 64;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer --
+    // ------------------------------------------------- operand producer --
     if (lane == 0) {
+      const uint32_t leader_full = mapa_shared(bar_full, 0);
       int stage = 0;
       uint32_t phase = 0;
       for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
         int tm, tn;
         tile_coords(p, t, tm, tn);
         const int band_a = 2 * tm + (int)rank;
-        const bool a_ok = band_a < p.bands_a;
-        const bool b1_ok = 2 * tn + 1 < p.bands_b;
-        const uint32_t tx = A_BYTES + B_BYTES + (a_ok ? SFA_BYTES : 0) + SF_BAND_BYTES + (b1_ok ? SF_BAND_BYTES : 0);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_cluster(bar_empty + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
-          const uint32_t full = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(full, tx);
-          tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, band_a * BM, full);
-          tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN + (int)rank * BN_CTA, full);
-          if (a_ok)
-            bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
-                      p.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
-          const uint8_t* sb0 = p.sfb + ((int64_t)(2 * tn) * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
-          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SF_BAND_BYTES, full);
-          if (b1_ok)
-            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SF_BAND_BYTES, sb0 + atoms_per_band * 512, SF_BAND_BYTES,
-                      full);
+          // The leader arms its barrier for both CTAs' bytes; the peer's
+          // copies may land before or after that, either is fine.
+          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (A_BYTES + B_BYTES));
+          tma_load_2d_pair(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, band_a * BM, leader_full + 8 * stage);
+          tma_load_2d_pair(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN + (int)rank * BN_CTA,
+                           leader_full + 8 * stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-      }
-      // Let in-flight copies land before the CTA can exit: wait (bounded)
-      // for the last phase issued on every stage.
-      for (int s = 0; s < STAGES; ++s) {
-        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-        mbar_wait(bar_full + 8 * s, par, p.status, 100000000ull);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------- MMA issuer (leader CTA) --
-    // The whole warp runs the loop and waits (one bounded wait per stage, on
-    // the scale-done barrier, which both CTAs' scale writers reach only after
-    // their stage data has landed); one elected lane issues the MMAs.  A
-    // single-lane loop with two waits per stage measured ~40% slower.
+    // The whole warp runs the loop and waits (bounded spins inside single asm
+    // blocks, decisions made warp-uniform by a vote); one elected lane issues
+    // the MMAs.  A single-lane issue loop with two waits per stage held the
+    // tensor pipe to ~180 cycles per 128-cycle MMA.
     if (rank == 0) {
       const bool leader = elect_one();
       int stage = 0;
@@ -245,7 +243,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         if (!ok) break;
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_sf + 8 * stage, phase, p.status));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_full + 8 * stage, phase, p.status) &&
+                                           mbar_wait_spin(bar_sf + 8 * stage, phase, p.status));
           if (!ok) break;
           tc_fence_after();
           if (leader) {
@@ -276,6 +275,39 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       if (leader) tc_commit_pair(bar_mma_done, 0x3);
       __syncwarp();
     }
+  } else if (warp == SF_PRODUCER_WARP) {
+    // --------------------------------------------------- scale producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
+        int tm, tn;
+        tile_coords(p, t, tm, tn);
+        const int band_a = 2 * tm + (int)rank;
+        const bool a_ok = band_a < p.bands_a;
+        const bool b1_ok = 2 * tn + 1 < p.bands_b;
+        const uint32_t tx = (a_ok ? SFA_BYTES : 0) + SF_BAND_BYTES + (b1_ok ? SF_BAND_BYTES : 0);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_sf_free + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
+          const uint32_t full = bar_sf_full + 8 * stage;
+          mbar_arrive_expect_tx(full, tx);
+          if (a_ok)
+            bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
+                      p.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
+          const uint8_t* sb0 = p.sfb + ((int64_t)(2 * tn) * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
+          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SF_BAND_BYTES, full);
+          if (b1_ok)
+            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SF_BAND_BYTES, sb0 + atoms_per_band * 512, SF_BAND_BYTES,
+                      full);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Let in-flight scale copies land before the CTA can exit.
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        mbar_wait(bar_sf_full + 8 * s, par, p.status, 100000000ull);
+      }
+    }
   } else if (warp < FIRST_EPI_WARP) {
     // ---------------------------------------------------- scale writers --
     // Quadrant q (= warp % 4) lanes 32q + r.  Scale atom row r holds the four
@@ -294,7 +326,15 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       const bool b1_ok = 2 * tn + 1 < p.bands_b;
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(bar_full + 8 * stage, phase, p.status)) { *abort_flag = 1; ok = false; break; }
+        // the stage's scale atoms are in shared memory, and its scale
+        // columns are free (the MMAs that last used them have completed)
+        if (!mbar_wait(bar_sf_full + 8 * stage, phase, p.status) ||
+            !mbar_wait_cluster(bar_empty + 8 * stage, phase ^ 1u, p.status)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const uint8_t* sfa_s = smem + OFF_SFA + stage * SFA_BYTES + lane * 16;
         const uint8_t* sfb_s = smem + OFF_SFB + stage * SFB_BYTES + lane * 16;
         uint32_t va[16], vb[32];
@@ -309,6 +349,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
           vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
           vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf_free + 8 * stage);  // the slot's shared memory may be refilled
         const uint32_t col = tmem_base + lane_off + 256u + (uint32_t)(stage * SF_COLS_PER_STAGE);
         tmem_st_32x32b_x16(col, va);
         tmem_st_32x32b_x16(col + 16, vb);
@@ -395,6 +437,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   __syncthreads();
   if (threadIdx.x == 0) {
     mbar_wait_cluster(bar_mma_done, 0, p.status, 10000000000ull);
+    // After an abort this CTA's operand copies (which complete on the
+    // leader's barrier, not on one it can watch) may still be in flight:
+    // give them time to land in its shared memory before it can exit.
+    if (*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 200000ull) {}
+    }
     mbar_arrive_cluster(mapa_shared(bar_exit, rank ^ 1u));
     mbar_wait_cluster(bar_exit, 0, p.status, 10000000000ull);
   }
