@@ -382,19 +382,22 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       tc_fence_after();
       int tm, tn;
       tile_coords(p, t, tm, tn);
-      // Pull this warp's 32 x 128 accumulator block out of tensor memory in
-      // 32-column chunks, scaling and rounding each into 16 packed bf16x2
-      // words; release the accumulator as soon as the last chunk is in
-      // registers so the next tile's MMAs overlap the stores.
+      // Pull this warp's 32 x 128 accumulator block out of tensor memory
+      // (two 32-column loads per wait), scaling and rounding into 64 packed
+      // bf16x2 words; release the accumulator as soon as the last chunk is
+      // in registers so the next tile's MMAs overlap the stores.
       uint32_t w[64];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + 32 * ch, v);
+      for (int pr = 0; pr < 2; ++pr) {  // two loads in flight per wait
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr + 64 * pr, v0);
+        tmem_ld_32x32b_x32(taddr + 64 * pr + 32, v1);
         tc_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          w[16 * ch + q] = scale_pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), alpha);
+        for (int q = 0; q < 16; ++q) {
+          w[32 * pr + q] = scale_pack_bf16x2(__uint_as_float(v0[2 * q]), __uint_as_float(v0[2 * q + 1]), alpha);
+          w[32 * pr + 16 + q] = scale_pack_bf16x2(__uint_as_float(v1[2 * q]), __uint_as_float(v1[2 * q + 1]), alpha);
+        }
       }
       tc_fence_before();
       __syncwarp();
