@@ -198,41 +198,21 @@ __device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
 }
 
 // Random words of the 8 pairs q0 .. q0 + 7 of a 16-element block (q0 a
-// multiple of 8): w_j = mix32(hk ^ lo32(q0 + j)), with hk = mix32(key ^
-// hi32(q0)).  Because j only touches the low 3 bits, the first xorshift is
-// shared (x ^ (x >> 16) = B ^ j with B = base ^ (base >> 16)) and the first
-// multiply splits into a shared part plus a 3-bit part.  Shifts right are
-// written as high products so most of the work runs on the multiply-add
-// pipe rather than the integer-logic pipe.
+// multiple of 8, so the pairs share hi32 and hk).
 __device__ __forceinline__ void sr_words8(uint32_t hk, uint32_t q0lo, uint32_t (&w)[8]) {
-  const uint32_t base = hk ^ q0lo;
-  const uint32_t b1 = base ^ __umulhi(base, 1u << 16);
-  const uint32_t hi = (b1 & ~7u) * 0x7feb352du;
-  const uint32_t lo3 = b1 & 7u;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t x = hi + (lo3 ^ (uint32_t)j) * 0x7feb352du;
-    x ^= __umulhi(x, 1u << 17);  // x >> 15
-    x *= 0x846ca68bu;
-    x ^= __umulhi(x, 1u << 16);  // x >> 16
-    w[j] = x;
-  }
+  for (int j = 0; j < 8; ++j) w[j] = mix32(hk ^ (q0lo + (uint32_t)j));
 }
 
-// SR codes (sign included, 4 bits each) of two values s0, s1 (already
-// scaled by the block's encoding factor) from one random word r: s0 uses the
-// low half-word, s1 the high half-word.  Returns c0 | c1 << 4.
+// SR codes (sign included) of two values s0, s1 (already scaled by the
+// block's encoding factor) from one random word r: s0 uses the low
+// half-word, s1 the high half-word.  Returns c0 | c1 << 4.  (Moving the
+// threshold and packing arithmetic onto high products and multiply-adds
+// measured slower.)
 __device__ __forceinline__ uint32_t sr_pair_codes(float s0, float s1, uint32_t r) {
-  const uint32_t u_hi = __umulhi(r, 1u << 16);                      // r >> 16
-  const uint32_t n1 = 0x3FFFFFu - u_hi * 64u;                       // 2^22 - 1 - 64 u_odd
-  const uint32_t n0 = 0x3FFFFFu - r * 64u + u_hi * (1u << 22);      // 2^22 - 1 - 64 (r & 0xFFFF)
-  const uint32_t b0 = __float_as_uint(__fmul_ru(fabsf(s0), 0x1p-126f));
-  const uint32_t b1 = __float_as_uint(__fmul_ru(fabsf(s1), 0x1p-126f));
-  const uint32_t c0 = min(__umulhi(b0 + n0, 1u << 10), 7u);        // (b0 + n0) >> 22, saturated
-  const uint32_t c1 = min(__umulhi(b1 + n1, 1u << 10), 7u);
-  const uint32_t g0 = __umulhi(__float_as_uint(s0), 2u);            // sign bits
-  const uint32_t g1 = __umulhi(__float_as_uint(s1), 2u);
-  return c0 + c1 * 16u + g0 * 8u + g1 * 128u;
+  const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
+  const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
+  return c0 | (c1 << 4);
 }
 
 // SR codes of 16 values already multiplied by the block's encoding factor.
