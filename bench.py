@@ -232,6 +232,7 @@ def run_ours(args):
     value = world * STEP_FLOPS / (ms_step * 1e-3) / 1e12
     e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    context = cublas_context(device) if (rank == 0 and not args.no_context) else None
     clocks = clk.summary()
 
     if rank == 0:
@@ -269,6 +270,7 @@ def run_ours(args):
                          "algorithmic_bytes": GEMM_FPROP_BYTES,
                          "traffic": traffic},
             "cpu_baseline": cpu,
+            "library_context": context,
             "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clocks,
@@ -404,6 +406,100 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- sweep --
+def run_sweep(args):
+    """Quantise-only sweep: bf16 tensors of 2^20 .. 2^30 elements (4096 rows,
+    N(0,1) with 0.1% x100 outliers) in the modes 1D RNE, 2D 16x16, RHT + SR
+    (transposed), plus 1D with the amax supplied (single pass).  One JSON
+    line per (size, mode): CUDA-event time with the L2 flushed between
+    repetitions, algorithmic GB/s and its fraction of the measured HBM copy
+    bandwidth."""
+    import nvfp4_block_scaled_27_b300 as nv
+    from workloads import SWEEP_LOG2, sweep_spec
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    nv.load_library()
+    peaks, _ = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for lg in SWEEP_LOG2:
+        spec = sweep_spec(lg)
+        x = make_bf16(spec, device=dev)
+        R, C = spec.rows, spec.cols
+        ain = x.abs().max().float().reshape(1)
+        o_row = nv.empty_nvfp4(R, C, device=dev)
+        o_col = nv.empty_nvfp4(C, R, device=dev)
+        torch.cuda.synchronize()  # inputs were made on the default stream; the timed calls run on `stream`
+        modes = {
+            "1d_rne": lambda: nv.nvfp4_quantize(x, nv.BLOCK_1D, 0, None, o_row, stream),
+            "1d_rne_amax_supplied": lambda: nv.nvfp4_quantize(x, nv.BLOCK_1D, 0, ain, o_row, stream),
+            "2d": lambda: nv.nvfp4_quantize(x, nv.BLOCK_2D, 0, None, o_row, stream),
+            "rht_sr_transposed": lambda: nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(3), None,
+                                                                  o_col, stream),
+        }
+        for name, fn in modes.items():
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    fn()
+                ev = []
+                for _ in range(args.steps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    ev.append((e0, e1))
+            stream.synchronize()
+            nv.check_status(stream)
+            ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+            gbs = QUANT_BYTES_PER_ELEM * R * C / (ms * 1e-3) / 1e9
+            print(json.dumps({"sweep": f"2^{lg}", "rows": R, "cols": C, "mode": name, "ms_median": round(ms, 4),
+                              "gbs_algorithmic": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}),
+                  flush=True)
+        del x, o_row, o_col
+
+
+# ---------------------------------------------------- library context --
+def cublas_context(device):
+    """The same three GEMM shapes in BF16 (torch.matmul -> cuBLAS) and FP8
+    E4M3 (torch._scaled_mm -> cuBLASLt), CUDA-event timed: context for the
+    NVFP4 GEMMs, not a target.  Entries that the installed torch cannot run
+    are null."""
+    shapes = {"fprop": (T, F2, H), "dgrad": (T, H, F), "wgrad": (F, H, T)}
+    out = {}
+    g = torch.Generator(device=device).manual_seed(0)
+    for name, (M, N, K) in shapes.items():
+        a = torch.randn(M, K, generator=g, device=device, dtype=torch.bfloat16)
+        b = torch.randn(N, K, generator=g, device=device, dtype=torch.bfloat16)
+        res = {}
+        for kind in ("bf16", "fp8_e4m3"):
+            try:
+                if kind == "bf16":
+                    fn = lambda: torch.matmul(a, b.t())
+                else:
+                    a8 = a.to(torch.float8_e4m3fn)
+                    b8 = b.to(torch.float8_e4m3fn)
+                    one = torch.ones((), device=device, dtype=torch.float32)
+                    fn = lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+                for _ in range(3):
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(5):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / 5
+                res[kind] = {"ms": round(ms, 4), "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}
+            except Exception as exc:  # noqa: BLE001 - context only
+                res[kind] = {"unavailable": type(exc).__name__}
+        out[name] = res
+        del a, b
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------- kernel cases --
 def _parse_case(spec):
     """`gemm:M,N,K` or `quant:MODE:ROWS,COLS` (MODE in 1d, 1d_sr, 2d, 2d_t,
@@ -486,12 +582,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="quantise-only sweep, 2^20 .. 2^30 elements")
+    ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS BF16/FP8 context timings")
     ap.add_argument("--case", action="append", default=[],
                     help="time single ops instead of the step: gemm:M,N,K or quant:MODE:ROWS,COLS")
     args = ap.parse_args()
-    if args.warmup < 3 and not args.case:
+    if args.warmup < 3 and not (args.case or args.sweep):
         args.warmup = 3
-    if args.case:
+    if args.sweep:
+        run_sweep(args)
+    elif args.case:
         run_cases(args)
     elif args.impl == "reference":
         run_reference(args)
