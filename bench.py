@@ -5,7 +5,9 @@ Llama 3 8B MLP at 32768 tokens (sequence 8192 x batch 4):
   fprop : X [32768, 4096] 1D RNE, gate+up W [28672, 4096] 2D  -> Y = X W^T
   dgrad : dY [32768, 14336] 1D SR, W [14336, 4096] 2D transposed -> dX = dY W
   wgrad : dY^T and X^T with the 16-point RHT + SR (same RHT seed)  -> dW = dY^T X
-i.e. 6 quantisations (amax pass + encode each) and 3 block-scaled GEMMs.
+i.e. 4 quantisation calls (X and dY each in one dual-orientation pass that
+yields the row-wise and the transposed RHT+SR operand; W and W^T 2D), each an
+amax pass + an encode kernel, and 3 block-scaled GEMMs.
 
 Printed metric: NVFP4 GEMM TFLOP/s of the step (GEMM flops / step time,
 quantisation included) on rank 0, one JSON line.  Kernel-level numbers (GEMM
@@ -110,7 +112,13 @@ class ClockSampler:
 
 
 class MlpStep:
-    """Device buffers and the launch sequence of one fwd+bwd MLP step."""
+    """Device buffers and the launch sequence of one fwd+bwd MLP step.
+
+    X and dY each feed two GEMMs (fprop/wgrad, dgrad/wgrad), so each is
+    quantised once per orientation by one dual-orientation call: the row-wise
+    operand (X: RNE, dY: stochastic rounding) and the transposed RHT + SR
+    operand for wgrad (same RHT seed for both).  W (gate+up) is quantised 2D
+    for fprop, the down-projection W 2D and transposed for dgrad."""
 
     def __init__(self, nv, device):
         self.nv = nv
@@ -121,15 +129,16 @@ class MlpStep:
         self.w2 = make_bf16(LLAMA3_8B_W_BWD, device=device)    # [F, H]
         e = nv.empty_nvfp4
         self.qx = e(T, H, device=device)
+        self.qxt = e(H, T, device=device)
         self.qw = e(F2, H, device=device)
         self.qdy = e(T, F, device=device)
-        self.qw2t = e(H, F, device=device)
         self.qdyt = e(F, T, device=device)
-        self.qxt = e(H, T, device=device)
+        self.qw2t = e(H, F, device=device)
         self.y = torch.empty(T, F2, dtype=torch.bfloat16, device=device)
         self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.dw = torch.empty(F, H, dtype=torch.bfloat16, device=device)
-        self.launches_per_step = 6 * 2 + 3
+        # kernels per step: 2 per quantisation call (amax pass + encode), 3 GEMMs
+        self.launches_per_step = 4 * 2 + 3
 
     def run(self, stream, gemm_events=None, quant_events=None):
         nv = self.nv
@@ -148,23 +157,23 @@ class MlpStep:
             if gemm_events is not None:
                 gemm_events[ev_i][1].record(stream)
 
-        # fprop
-        q(0, lambda: nv.nvfp4_quantize(self.x, nv.BLOCK_1D, 0, None, self.qx, stream))
+        # fprop (X's transposed operand for wgrad comes out of the same pass)
+        q(0, lambda: nv.nvfp4_quantize_dual(self.x, nv.ROUND_RNE, 0, RHT_SEED, sr_seed(2), None, None, self.qx,
+                                            self.qxt, stream))
         q(1, lambda: nv.nvfp4_quantize(self.w, nv.BLOCK_2D, 0, None, self.qw, stream))
         g(0, self.qx, self.qw, self.y)
-        # dgrad
-        q(2, lambda: nv.nvfp4_quantize(self.dy, nv.ROUND_SR, sr_seed(0), None, self.qdy, stream))
+        # dgrad (dY's transposed operand for wgrad comes out of the same pass)
+        q(2, lambda: nv.nvfp4_quantize_dual(self.dy, nv.ROUND_SR, sr_seed(0), RHT_SEED, sr_seed(1), None, None,
+                                            self.qdy, self.qdyt, stream))
         q(3, lambda: nv.nvfp4_quantize(self.w2, nv.BLOCK_2D | nv.TRANSPOSE_OUT, 0, None, self.qw2t, stream))
         g(1, self.qdy, self.qw2t, self.dx)
         # wgrad
-        q(4, lambda: nv.nvfp4_quantize_rht_sr(self.dy, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(1), None, self.qdyt,
-                                             stream))
-        q(5, lambda: nv.nvfp4_quantize_rht_sr(self.x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(2), None, self.qxt,
-                                             stream))
         g(2, self.qdyt, self.qxt, self.dw)
 
-    quant_elems = [T * H, F2 * H, T * F, F * H, T * F, T * H]
-    quant_names = ["X 1D", "W 2D", "dY 1D SR", "W^T 2D", "dY^T RHT+SR", "X^T RHT+SR"]
+    quant_elems = [T * H, F2 * H, T * F, F * H]
+    quant_names = ["X dual (1D RNE + RHT/SR transposed)", "W 2D", "dY dual (1D SR + RHT/SR transposed)", "W^T 2D"]
+    # algorithmic bytes per element: read 2 B; write 0.5625 B per output operand
+    quant_bytes_per_elem = [2.0 + 2 * 0.5625, QUANT_BYTES_PER_ELEM, 2.0 + 2 * 0.5625, QUANT_BYTES_PER_ELEM]
 
 
 def run_ours(args):
@@ -189,7 +198,7 @@ def run_ours(args):
     stream.synchronize()
     nv.check_status(stream)
 
-    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(6)]
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
     gemm_ev = [mk()[:3] for _ in range(args.steps)]
     quant_ev = [mk() for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -217,11 +226,11 @@ def run_ours(args):
     gemm_ms = {n: statistics.mean(gemm_ev[k][i][0].elapsed_time(gemm_ev[k][i][1]) for k in range(args.steps))
                for i, n in enumerate(["fprop", "dgrad", "wgrad"])}
     quant_ms = [statistics.mean(quant_ev[k][i][0].elapsed_time(quant_ev[k][i][1]) for k in range(args.steps))
-                for i in range(6)]
+                for i in range(len(step.quant_elems))]
     gemm_total_ms = sum(gemm_ms.values())
     fprop_tflops = GEMM_FLOPS["fprop"] / (gemm_ms["fprop"] * 1e-3) / 1e12
     gemm_tflops = STEP_FLOPS / (gemm_total_ms * 1e-3) / 1e12
-    quant_bytes = sum(QUANT_BYTES_PER_ELEM * n for n in step.quant_elems)
+    quant_bytes = sum(b * n for b, n in zip(step.quant_bytes_per_elem, step.quant_elems))
     quant_gbs = quant_bytes / (sum(quant_ms) * 1e-3) / 1e9
 
     peaks, peak_src = _peaks()
@@ -254,10 +263,11 @@ def run_ours(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "gemm": {n: {"ms": round(v, 4), "tflops": round(GEMM_FLOPS[n] / (v * 1e-3) / 1e12, 1)}
                      for n, v in gemm_ms.items()},
-            "quantize": [{"tensor": nm, "ms": round(t, 4),
-                          "gbs": round(QUANT_BYTES_PER_ELEM * n / (t * 1e-3) / 1e9, 1),
-                          "frac_hbm": round(QUANT_BYTES_PER_ELEM * n / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
-                         for nm, n, t in zip(step.quant_names, step.quant_elems, quant_ms)],
+            "quantize": [{"call": nm, "ms": round(t, 4),
+                          "gbs": round(bpe * n / (t * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(bpe * n / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+                         for nm, n, bpe, t in zip(step.quant_names, step.quant_elems, step.quant_bytes_per_elem,
+                                                  quant_ms)],
             "quantize_gbs_all": round(quant_gbs, 1),
             "roofline": {"kernel": "nvfp4_gemm_kernel, Llama 3 8B MLP fprop launch (M=32768, N=28672, K=4096)",
                          "bound": "tensor", "achieved": round(fprop_tflops, 1),

@@ -131,6 +131,27 @@ int nvfp4_quantize_rht_sr(const void* x, int64_t rows, int64_t cols, int64_t ld,
                           const float* amax_in, const nvfp4_tensor* out,
                           nvfp4_stream_t stream);
 
+/* Dual-orientation quantisation: one pass over x [rows, cols] produces both
+ * operands a training step takes from the same tensor (the activations X
+ * feed fprop and wgrad, the output gradient dY feeds dgrad and wgrad):
+ *   out_row [rows, cols]  = nvfp4_quantize(x, row_flags, row_sr_seed, amax_row_in)
+ *                           with 1D blocks (row_flags: NVFP4_ROUND_RNE or
+ *                           NVFP4_ROUND_SR; nothing else),
+ *   out_col [cols, rows]  = nvfp4_quantize_rht_sr(x, NVFP4_TRANSPOSE_OUT,
+ *                           rht_seed, col_sr_seed, amax_col_in),
+ * bit-identical to those two calls.  The recipe's data flow inside the MLP
+ * GEMMs (readjensen.com NVFP4 training-recipe article, MLP data-flow
+ * paragraph) quantises each of X and dY once per orientation; this call reads
+ * x twice (one pass for both amaxes unless both are supplied, one for both
+ * encodings) instead of four times.  Both outputs must use the same scale
+ * layout.  Requirements: rows % 16 == 0 and cols % 16 == 0 (% 64 for the MMA
+ * layout), x 16-byte aligned, ld % 8 == 0, codes 8-byte aligned.  Returns
+ * NVFP4_OK or a negative status code; nothing is launched on an error. */
+int nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, uint32_t row_flags,
+                        uint64_t row_sr_seed, uint64_t rht_seed, uint64_t col_sr_seed,
+                        const float* amax_row_in, const float* amax_col_in, const nvfp4_tensor* out_row,
+                        const nvfp4_tensor* out_col, nvfp4_stream_t stream);
+
 /* Block-scaled NVFP4 GEMM, "TN": C[M, N] = s_gA * s_gB * A[M, K] * B[N, K]^T
  * with fp32 accumulation and a BF16 (round-to-nearest-even) result.
  * A and B must use NVFP4_SCALES_MMA, K = A->cols = B->cols, K % 256 == 0.

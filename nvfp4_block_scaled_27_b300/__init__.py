@@ -42,7 +42,7 @@ SCALES_CANONICAL = 0
 SCALES_MMA = 1
 
 EXPORTED = (
-    "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_gemm",
+    "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_quantize_dual", "nvfp4_gemm",
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3",
 )
@@ -85,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_quantize.argtypes = [vp, i64, i64, i64, u32, u64, vp, tp, vp]
     L.nvfp4_quantize_rht_sr.restype = ctypes.c_int
     L.nvfp4_quantize_rht_sr.argtypes = [vp, i64, i64, i64, u32, u64, u64, vp, tp, vp]
+    L.nvfp4_quantize_dual.restype = ctypes.c_int
+    L.nvfp4_quantize_dual.argtypes = [vp, i64, i64, i64, u32, u64, u64, u64, vp, vp, tp, tp, vp]
     L.nvfp4_gemm.restype = ctypes.c_int
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, vp]
     L.nvfp4_check_status.restype = ctypes.c_int
@@ -181,6 +183,19 @@ def nvfp4_quantize_rht_sr(x: torch.Tensor, flags: int, rht_seed: int, sr_seed: i
     _check(rc, "nvfp4_quantize_rht_sr")
 
 
+def nvfp4_quantize_dual(x: torch.Tensor, row_flags: int, row_sr_seed: int, rht_seed: int, col_sr_seed: int,
+                        amax_row_in, amax_col_in, out_row: NVFP4Tensor, out_col: NVFP4Tensor, stream=None) -> None:
+    _require_cuda(x)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise Nvfp4Error("x must be a 2-D bf16 tensor with unit column stride")
+    cr, cc = out_row.c_struct(), out_col.c_struct()
+    rc = load_library().nvfp4_quantize_dual(
+        x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), row_flags, row_sr_seed, rht_seed, col_sr_seed,
+        None if amax_row_in is None else amax_row_in.data_ptr(), None if amax_col_in is None else amax_col_in.data_ptr(),
+        ctypes.byref(cr), ctypes.byref(cc), _stream(stream))
+    _check(rc, "nvfp4_quantize_dual")
+
+
 def nvfp4_gemm(a: NVFP4Tensor, b: NVFP4Tensor, c: torch.Tensor, stream=None) -> None:
     _require_cuda(c)
     if c.dtype != torch.bfloat16 or c.dim() != 2 or c.stride(1) != 1:
@@ -233,6 +248,18 @@ def quantize_rht_sr(x: torch.Tensor, flags: int = TRANSPOSE_OUT, rht_seed: int =
         out = empty_nvfp4(orows, ocols, layout, x.device)
     nvfp4_quantize_rht_sr(x, flags, rht_seed, sr_seed, amax_in, out, stream)
     return out
+
+
+def quantize_dual(x: torch.Tensor, row_flags: int = 0, row_sr_seed: int = 0, rht_seed: int = 0, col_sr_seed: int = 0,
+                  amax_row_in=None, amax_col_in=None, layout: int = SCALES_MMA, stream=None):
+    """Row-wise 1D operand and transposed RHT + SR operand of x from one pass;
+    returns (out_row [rows, cols], out_col [cols, rows])."""
+    rows, cols = x.shape
+    out_row = empty_nvfp4(rows, cols, layout, x.device)
+    out_col = empty_nvfp4(cols, rows, layout, x.device)
+    nvfp4_quantize_dual(x, row_flags, row_sr_seed, rht_seed, col_sr_seed, amax_row_in, amax_col_in, out_row, out_col,
+                        stream)
+    return out_row, out_col
 
 
 def gemm(a: NVFP4Tensor, b: NVFP4Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

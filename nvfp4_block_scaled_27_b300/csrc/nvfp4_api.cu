@@ -133,6 +133,50 @@ int nvfp4_quantize_rht_sr(const void* x, int64_t rows, int64_t cols, int64_t ld,
                          stream);
 }
 
+int nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, uint32_t row_flags,
+                        uint64_t row_sr_seed, uint64_t rht_seed, uint64_t col_sr_seed, const float* amax_row_in,
+                        const float* amax_col_in, const nvfp4_tensor* out_row, const nvfp4_tensor* out_col,
+                        nvfp4_stream_t stream) {
+  if (row_flags & ~NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;  // 1D blocks, no transpose
+  int rc = check_tensor_buffers(out_row);
+  if (rc) return rc;
+  rc = check_tensor_buffers(out_col);
+  if (rc) return rc;
+  if (out_row->scale_layout != out_col->scale_layout) return NVFP4_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols) return NVFP4_ERR_INVALID_ARG;
+  if (out_row->rows != rows || out_row->cols != cols || out_col->rows != cols || out_col->cols != rows)
+    return NVFP4_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || rows % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (out_row->scale_layout == NVFP4_SCALES_MMA && (cols % 64 != 0 || rows % 64 != 0)) return NVFP4_ERR_INVALID_ARG;
+  if (ld % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (rows * (cols / 8)) >= (int64_t)1 << 31) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  rc = check_device(&dev);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rows == 0 || cols == 0) {
+    // empty tensor: both operands as the separate calls leave them
+    for (int k = 0; k < 2; ++k) {
+      const nvfp4_tensor* o = k ? out_col : out_row;
+      const float* ain = k ? amax_col_in : amax_row_in;
+      if (ain) {
+        if (cudaMemcpyAsync(o->amax, ain, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+      } else if (cudaMemsetAsync(o->amax, 0, sizeof(float), s) != cudaSuccess) {
+        return NVFP4_ERR_CUDA;
+      }
+      if (cudaMemsetAsync(o->global_scale, 0, sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+      const size_t sb = nvfp4_scales_bytes(o->rows, o->cols, o->scale_layout);
+      if (sb && cudaMemsetAsync(o->scales, 0, sb, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+  }
+  if (!x || !aligned16(x)) return NVFP4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(out_row->codes) & 7u) != 0 || (reinterpret_cast<uintptr_t>(out_col->codes) & 7u) != 0)
+    return NVFP4_ERR_INVALID_ARG;
+  return nvfp4::quantize_dual_launch(*dev, x, rows, cols, ld, (row_flags & NVFP4_ROUND_SR) != 0, row_sr_seed, rht_seed,
+                                     col_sr_seed, amax_row_in, amax_col_in, *out_row, *out_col, s);
+}
+
 int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc, nvfp4_stream_t stream) {
   int rc = check_tensor_buffers(A);
   if (rc) return rc;

@@ -26,6 +26,12 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
                     uint32_t flags, bool rht, uint64_t rht_seed, uint64_t sr_seed,
                     const float* amax_in, const nvfp4_tensor& out, cudaStream_t stream);
 
+// Dual-orientation quantiser entry (arguments validated by the caller).
+int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                         bool row_sr, uint64_t row_sr_seed, uint64_t rht_seed, uint64_t col_sr_seed,
+                         const float* amax_row_in, const float* amax_col_in, const nvfp4_tensor& out_row,
+                         const nvfp4_tensor& out_col, cudaStream_t stream);
+
 // GEMM entry (arguments validated by the caller).
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
                 int64_t ldc, cudaStream_t stream);

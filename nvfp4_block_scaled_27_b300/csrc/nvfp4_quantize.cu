@@ -182,6 +182,63 @@ __global__ void __launch_bounds__(256) amax_rht_cols_kernel(const uint16_t* __re
   cta_amax_commit(m, out);
 }
 
+// Two CTA-wide maxima at once (one shared scratch, one barrier), then one
+// atomicMax each.
+__device__ __forceinline__ void cta_amax_commit2(uint32_t m1, float* out1, uint32_t m2, float* out2) {
+  __shared__ uint32_t red2[2][32];
+  m1 = warp_max_u32(m1);
+  m2 = warp_max_u32(m2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red2[0][warp] = m1;
+    red2[1][warp] = m2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const bool in = lane < (int)(blockDim.x >> 5);
+    m1 = warp_max_u32(in ? red2[0][lane] : 0u);
+    m2 = warp_max_u32(in ? red2[1][lane] : 0u);
+    if (lane == 0) {
+      if (m1 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out1), m1);
+      if (m2 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out2), m2);
+    }
+  }
+}
+
+// Both amaxes the dual-orientation quantiser needs, from one read: the plain
+// amax (row-wise operand) and the amax after the column-wise transform
+// (transposed operand).  A thread owns 16 rows x 8 columns.
+__global__ void __launch_bounds__(256) amax_dual_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                        int64_t ld, uint32_t signs, float* out_plain,
+                                                        float* out_rht) {
+  uint32_t mp = 0u, mr = 0u;
+  const uint32_t nv = (uint32_t)(cols / 8);
+  const uint32_t total = (uint32_t)((rows / 16) * nv);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t rc = i / nv, vc = i - rc * nv;
+    const uint16_t* base = x + (int64_t)rc * 16 * ld + (int64_t)vc * 8;
+    uint4 u[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) u[k] = ldg_nc(base + (int64_t)k * ld);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) mp = absmax_pairs(mp, u[k]);
+#pragma unroll
+    for (int c = 0; c < 8; c += 2) {
+      float v0[16], v1[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t w = (c < 2) ? u[k].x : (c < 4) ? u[k].y : (c < 6) ? u[k].z : u[k].w;
+        v0[k] = bf16_lo(w);
+        v1[k] = bf16_hi(w);
+      }
+      rht16x2(v0, v1, signs);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) mr = max(mr, max(__float_as_uint(fabsf(v0[k])), __float_as_uint(fabsf(v1[k]))));
+    }
+  }
+  cta_amax_commit2(pairs_to_f32_bits(mp), out_plain, mr, out_rht);
+}
+
 // ------------------------------------------------------- row-wise, 1D --
 template <bool kSR, bool kRHT, bool kMMA>
 __device__ __forceinline__ void quant_block_1d(const QuantParams& p, uint32_t i, uint32_t nb,
@@ -299,121 +356,194 @@ constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
 constexpr int kColTileCols = 256;  // input columns per tile
 constexpr int kColThreads = 128;   // one thread per column pair
 
-// Output row c = input column c, output column r = input row r.  Blocks run
-// along the input's rows; with kTwoD the 16x16 tile amax is shared by the 8
-// threads (16 columns) of a tile via shuffles.
+// Stage the tile (r0, c0) of the input in shared memory: a warp moves one
+// 512-byte input row segment per step; out-of-range elements read as 0.
+__device__ __forceinline__ void stage_tile(const QuantParams& p, uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                           int64_t r0, int64_t c0) {
+  const int tid = threadIdx.x;
+#pragma unroll 4
+  for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
+    const int idx = k * kColThreads + tid;
+    const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + row < p.rows && c0 + vec * 8 < p.cols) val = ldg_nc(p.x + (r0 + row) * p.ld + c0 + vec * 8);
+    *reinterpret_cast<uint4*>(&tile[row][vec * 4]) = val;
+  }
+}
+
+// Column-wise (transposed) quantisation of a staged tile.  Output row c =
+// input column c, output column r = input row r.  Blocks run along the
+// input's rows; with kTwoD the 16x16 tile amax is shared by the 8 threads
+// (16 columns) of a tile via shuffles.
+template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
+__device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                          int64_t r0, int64_t c0, float sg, float den) {
+  const int64_t R = p.rows, C = p.cols;
+  const int tid = threadIdx.x;
+  const int64_t kb_per_row = R / 16;  // output blocks per output row
+  const int64_t c = c0 + 2 * tid;  // this thread's two output rows: c, c + 1
+  const bool col_ok = c < C;
+  // Codes and scales of the tile's four 16-row chunks are collected and
+  // written together when the tile is whole: 32 contiguous code bytes per
+  // output row (two 16-byte stores) and one 32-bit word of four scales.
+  const bool whole = (r0 + kColTileRows <= R) && ((R & 31) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0);
+  uint2 qa[4], qb[4];
+  uint32_t sca = 0u, scb = 0u;
+#pragma unroll
+  for (int k = 0; k < kColTileRows / 16; ++k) {
+    const int64_t rb = r0 + 16 * k;  // first input row of the block
+    if (rb >= R) break;              // uniform across the CTA
+    float v0[16], v1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w = tile[16 * k + i][tid];
+      v0[i] = bf16_lo(w);
+      v1[i] = bf16_hi(w);
+    }
+    if (kRHT) rht16x2(v0, v1, p.rht_signs);
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      a0 = fmaxf(a0, fabsf(v0[i]));
+      a1 = fmaxf(a1, fabsf(v1[i]));
+    }
+    if (kTwoD) {
+      float a = fmaxf(a0, a1);
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+      a0 = a1 = a;
+    }
+    if (!col_ok) continue;
+    const uint32_t sc0 = block_scale_code(a0, den), sc1 = block_scale_code(a1, den);
+    const uint64_t e01 = f2_pack(block_enc(sg, sc0), block_enc(sg, sc1));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f2_unpack(f2_mul(f2_pack(v0[i], v1[i]), e01), v0[i], v1[i]);
+    uint2 q0, q1;
+    if (kSR) {
+      const uint64_t p0 = ((uint64_t)c * (uint64_t)R + (uint64_t)rb) >> 1;
+      const uint64_t p1 = ((uint64_t)(c + 1) * (uint64_t)R + (uint64_t)rb) >> 1;
+      q0 = encode16_sr_scaled(v0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
+      q1 = encode16_sr_scaled(v1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
+    } else {
+      q0 = encode16_rne_scaled(v0);
+      q1 = encode16_rne_scaled(v1);
+    }
+    qa[k] = q0;
+    qb[k] = q1;
+    sca |= sc0 << (8 * k);
+    scb |= sc1 << (8 * k);
+    if (!whole) {
+      *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
+      *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
+      const int64_t kb = rb / 16;
+      if (kMMA) {
+        p.scales[mma_scale_offset(c, kb, kb_per_row / 4)] = (uint8_t)sc0;
+        p.scales[mma_scale_offset(c + 1, kb, kb_per_row / 4)] = (uint8_t)sc1;
+      } else {
+        p.scales[c * kb_per_row + kb] = (uint8_t)sc0;
+        p.scales[(c + 1) * kb_per_row + kb] = (uint8_t)sc1;
+      }
+    }
+  }
+  if (whole && col_ok) {
+    uint8_t* o0 = p.codes + c * (R / 2) + r0 / 2;
+    uint8_t* o1 = o0 + R / 2;
+    *reinterpret_cast<uint4*>(o0) = make_uint4(qa[0].x, qa[0].y, qa[1].x, qa[1].y);
+    *reinterpret_cast<uint4*>(o0 + 16) = make_uint4(qa[2].x, qa[2].y, qa[3].x, qa[3].y);
+    *reinterpret_cast<uint4*>(o1) = make_uint4(qb[0].x, qb[0].y, qb[1].x, qb[1].y);
+    *reinterpret_cast<uint4*>(o1 + 16) = make_uint4(qb[2].x, qb[2].y, qb[3].x, qb[3].y);
+    const int64_t kb0 = r0 / 16;  // a multiple of 4: the four scales share one word
+    if (kMMA) {
+      *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c, kb0, kb_per_row / 4)) = sca;
+      *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c + 1, kb0, kb_per_row / 4)) = scb;
+    } else {
+      uint8_t* s0 = p.scales + c * kb_per_row + kb0;
+      uint8_t* s1 = s0 + kb_per_row;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s0[k] = (uint8_t)(sca >> (8 * k));
+        s1[k] = (uint8_t)(scb >> (8 * k));
+      }
+    }
+  }
+}
+
 template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) {
   __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
-  const int64_t R = p.rows, C = p.cols;
-  const int64_t tiles_r = (R + kColTileRows - 1) / kColTileRows;
-  const int64_t tiles_c = (C + kColTileCols - 1) / kColTileCols;
-  const int64_t ntiles = tiles_r * tiles_c;
+  const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);
+    __syncthreads();
+    cols_tile<kSR, kRHT, kTwoD, kMMA>(p, tile, tr * kColTileRows, tc * kColTileCols, sg, den);
+    __syncthreads();
+  }
+}
+
+// Row-wise 1D quantisation of a staged tile: thread t owns 16-column block
+// t % 16 of rows t / 16 + 8 i (i = 0..7); 16 threads write 128 contiguous
+// code bytes of a row.
+template <bool kSR, bool kMMA>
+__device__ __forceinline__ void rows_tile(const QuantParams& p, const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                          int64_t r0, int64_t c0, float sg, float den) {
   const int tid = threadIdx.x;
-  const int64_t kb_per_row = R / 16;  // output blocks per output row
+  const int blk = tid & 15;
+  const int64_t col = c0 + 16 * blk;
+  if (col >= p.cols) return;  // cols % 16 == 0: a block is wholly in or out
+  const int64_t nb = p.cols / 16;
+#pragma unroll 2
+  for (int i = 0; i < kColTileRows / 8; ++i) {
+    const int rl = (tid >> 4) + 8 * i;
+    const int64_t r = r0 + rl;
+    if (r >= p.rows) break;
+    const uint4 a = *reinterpret_cast<const uint4*>(&tile[rl][8 * blk]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&tile[rl][8 * blk + 4]);
+    float v[16];
+    unpack16(a, b, v);
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
+    const uint32_t sc = block_scale_code(amax_b, den);
+    const float enc = block_enc(sg, sc);
+    uint2 q;
+    if (kSR) {
+      const uint64_t q0 = ((uint64_t)r * (uint64_t)p.cols + (uint64_t)col) >> 1;
+      q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+    } else {
+      q = encode16_rne(v, enc);
+    }
+    *reinterpret_cast<uint2*>(p.codes + r * (p.cols / 2) + col / 2) = q;
+    const int64_t kb = col / 16;
+    p.scales[kMMA ? mma_scale_offset(r, kb, nb / 4) : r * nb + kb] = (uint8_t)sc;
+  }
+}
+
+// Dual-orientation quantisation: one read of each input tile produces the
+// row-wise 1D operand (pr: RNE or SR) and the transposed RHT + SR operand
+// (pc).  Results are bit-identical to the two separate kernels.
+template <bool kRowSR, bool kMMA>
+__global__ void __launch_bounds__(kColThreads) quant_dual_kernel(QuantParams pr, QuantParams pc) {
+  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  float amax_r, amax_c;
+  const float sg_r = tensor_scale(pr, amax_r);
+  const float sg_c = tensor_scale(pc, amax_c);
+  const float den_r = __fmul_rn(sg_r, 6.0f), den_c = __fmul_rn(sg_c, 6.0f);
+  const int64_t tiles_c = (pr.cols + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = ((pr.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
     const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
-    // stage the tile: a warp moves one 512-byte input row segment per step
-#pragma unroll 4
-    for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
-      const int idx = k * kColThreads + tid;
-      const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (r0 + row < R && c0 + vec * 8 < C) val = ldg_nc(p.x + (r0 + row) * p.ld + c0 + vec * 8);
-      *reinterpret_cast<uint4*>(&tile[row][vec * 4]) = val;
-    }
+    stage_tile(pr, tile, r0, c0);
     __syncthreads();
-    const int64_t c = c0 + 2 * tid;  // this thread's two output rows: c, c + 1
-    const bool col_ok = c < C;
-    // Codes and scales of the tile's four 16-row chunks are collected and
-    // written together when the tile is whole: 32 contiguous code bytes per
-    // output row (two 16-byte stores) and one 32-bit word of four scales.
-    const bool whole = (r0 + kColTileRows <= R) && ((R & 31) == 0) &&
-                       ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0);
-    uint2 qa[4], qb[4];
-    uint32_t sca = 0u, scb = 0u;
-#pragma unroll
-    for (int k = 0; k < kColTileRows / 16; ++k) {
-      const int64_t rb = r0 + 16 * k;  // first input row of the block
-      if (rb >= R) break;              // uniform across the CTA
-      float v0[16], v1[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t w = tile[16 * k + i][tid];
-        v0[i] = bf16_lo(w);
-        v1[i] = bf16_hi(w);
-      }
-      if (kRHT) rht16x2(v0, v1, p.rht_signs);
-      float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        a0 = fmaxf(a0, fabsf(v0[i]));
-        a1 = fmaxf(a1, fabsf(v1[i]));
-      }
-      if (kTwoD) {
-        float a = fmaxf(a0, a1);
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        a0 = a1 = a;
-      }
-      if (!col_ok) continue;
-      const uint32_t sc0 = block_scale_code(a0, den), sc1 = block_scale_code(a1, den);
-      const uint64_t e01 = f2_pack(block_enc(sg, sc0), block_enc(sg, sc1));
-#pragma unroll
-      for (int i = 0; i < 16; ++i) f2_unpack(f2_mul(f2_pack(v0[i], v1[i]), e01), v0[i], v1[i]);
-      uint2 q0, q1;
-      if (kSR) {
-        const uint64_t p0 = ((uint64_t)c * (uint64_t)R + (uint64_t)rb) >> 1;
-        const uint64_t p1 = ((uint64_t)(c + 1) * (uint64_t)R + (uint64_t)rb) >> 1;
-        q0 = encode16_sr_scaled(v0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
-        q1 = encode16_sr_scaled(v1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
-      } else {
-        q0 = encode16_rne_scaled(v0);
-        q1 = encode16_rne_scaled(v1);
-      }
-      qa[k] = q0;
-      qb[k] = q1;
-      sca |= sc0 << (8 * k);
-      scb |= sc1 << (8 * k);
-      if (!whole) {
-        *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
-        *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
-        const int64_t kb = rb / 16;
-        if (kMMA) {
-          p.scales[mma_scale_offset(c, kb, kb_per_row / 4)] = (uint8_t)sc0;
-          p.scales[mma_scale_offset(c + 1, kb, kb_per_row / 4)] = (uint8_t)sc1;
-        } else {
-          p.scales[c * kb_per_row + kb] = (uint8_t)sc0;
-          p.scales[(c + 1) * kb_per_row + kb] = (uint8_t)sc1;
-        }
-      }
-    }
-    if (whole && col_ok) {
-      uint8_t* o0 = p.codes + c * (R / 2) + r0 / 2;
-      uint8_t* o1 = o0 + R / 2;
-      *reinterpret_cast<uint4*>(o0) = make_uint4(qa[0].x, qa[0].y, qa[1].x, qa[1].y);
-      *reinterpret_cast<uint4*>(o0 + 16) = make_uint4(qa[2].x, qa[2].y, qa[3].x, qa[3].y);
-      *reinterpret_cast<uint4*>(o1) = make_uint4(qb[0].x, qb[0].y, qb[1].x, qb[1].y);
-      *reinterpret_cast<uint4*>(o1 + 16) = make_uint4(qb[2].x, qb[2].y, qb[3].x, qb[3].y);
-      const int64_t kb0 = r0 / 16;  // a multiple of 4: the four scales share one word
-      if (kMMA) {
-        *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c, kb0, kb_per_row / 4)) = sca;
-        *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c + 1, kb0, kb_per_row / 4)) = scb;
-      } else {
-        uint8_t* s0 = p.scales + c * kb_per_row + kb0;
-        uint8_t* s1 = s0 + kb_per_row;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s0[k] = (uint8_t)(sca >> (8 * k));
-          s1[k] = (uint8_t)(scb >> (8 * k));
-        }
-      }
-    }
+    rows_tile<kRowSR, kMMA>(pr, tile, r0, c0, sg_r, den_r);
+    cols_tile<true, true, false, kMMA>(pc, tile, r0, c0, sg_c, den_c);
     __syncthreads();
   }
 }
@@ -552,6 +682,67 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
       launch_cols<true, false, false>(dev, p, mma, stream);
     } else {
       launch_cols<false, false, false>(dev, p, mma, stream);
+    }
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// Dual-orientation quantisation (row-wise 1D + transposed RHT/SR).
+int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                         bool row_sr, uint64_t row_sr_seed, uint64_t rht_seed, uint64_t col_sr_seed,
+                         const float* amax_row_in, const float* amax_col_in, const nvfp4_tensor& out_row,
+                         const nvfp4_tensor& out_col, cudaStream_t stream) {
+  const uint32_t signs = rht_sign_bits(rht_seed);
+  QuantParams pr, pc;
+  for (QuantParams* q : {&pr, &pc}) {
+    q->x = static_cast<const uint16_t*>(x);
+    q->rows = rows;
+    q->cols = cols;
+    q->ld = ld;
+    q->status = dev.status;
+    q->rht_signs = signs;
+  }
+  pr.orows = out_row.rows; pr.ocols = out_row.cols; pr.codes = out_row.codes; pr.scales = out_row.scales;
+  pr.sg_out = out_row.global_scale; pr.sr_key = stream_key(row_sr_seed, kTagSR);
+  pc.orows = out_col.rows; pc.ocols = out_col.cols; pc.codes = out_col.codes; pc.scales = out_col.scales;
+  pc.sg_out = out_col.global_scale; pc.sr_key = stream_key(col_sr_seed, kTagSR);
+  const bool mma = out_row.scale_layout == NVFP4_SCALES_MMA;  // the caller checks both layouts agree
+
+  for (const nvfp4_tensor* o : {&out_row, &out_col}) {
+    if (o->scale_layout == NVFP4_SCALES_MMA && (o->rows % 128) != 0) {
+      const int64_t band = (o->cols / 64) * 512;
+      if (cudaMemsetAsync(o->scales + (o->rows / 128) * band, 0, band, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+  }
+  // Pass 1: both amaxes from one read (unless both are supplied).
+  if (!(amax_row_in && amax_col_in)) {
+    if (cudaMemsetAsync(out_row.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaMemsetAsync(out_col.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    amax_dual_kernel<<<grid_for(amax_dual_kernel, dev, (rows / 16) * (cols / 8), 256), 256, 0, stream>>>(
+        pr.x, rows, cols, ld, signs, out_row.amax, out_col.amax);
+  }
+  pr.amax_src = amax_row_in ? amax_row_in : out_row.amax;
+  pr.amax_out = amax_row_in ? out_row.amax : nullptr;
+  pc.amax_src = amax_col_in ? amax_col_in : out_col.amax;
+  pc.amax_out = amax_col_in ? out_col.amax : nullptr;
+
+  // Pass 2: one read, both outputs.
+  const int64_t tiles = ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
+  if (row_sr) {
+    if (mma) {
+      auto k = quant_dual_kernel<true, true>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+    } else {
+      auto k = quant_dual_kernel<true, false>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+    }
+  } else {
+    if (mma) {
+      auto k = quant_dual_kernel<false, true>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+    } else {
+      auto k = quant_dual_kernel<false, false>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
     }
   }
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;

@@ -81,8 +81,17 @@ def test_llama3_8b_dgrad_wgrad():
     dx = nv.gemm(qdy, qwt)
     torch.cuda.synchronize()
     _sample_check(dx, rdy, rwt, seed=1)
-    del qdy, rdy, dx
+    del qdy, dx
     qdyt, rdyt = _quant_and_check(dy, nv.TRANSPOSE_OUT, rht=True, seed=sr_seed(1), what="dY^T")
+    # the dual-orientation call produces both dY operands in one pass: same
+    # bits as the oracle's row-wise SR and transposed RHT + SR quantisations
+    d_row, d_col = nv.quantize_dual(dy, nv.ROUND_SR, row_sr_seed=sr_seed(0), rht_seed=RHT_SEED,
+                                    col_sr_seed=sr_seed(1))
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.OK
+    assert_quant_equal(d_row, rdy, "dual dY row")
+    assert_quant_equal(d_col, rdyt, "dual dY^T")
+    del d_row, d_col, rdy
     qxt, rxt = _quant_and_check(x, nv.TRANSPOSE_OUT, rht=True, seed=sr_seed(2), what="X^T")
     dw = nv.gemm(qdyt, qxt)
     torch.cuda.synchronize()
