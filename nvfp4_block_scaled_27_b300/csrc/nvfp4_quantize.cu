@@ -356,19 +356,26 @@ constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
 constexpr int kColTileCols = 256;  // input columns per tile
 constexpr int kColThreads = 128;   // one thread per column pair
 
-// Stage the tile (r0, c0) of the input in shared memory: a warp moves one
-// 512-byte input row segment per step; out-of-range elements read as 0.
+// Stage the tile (r0, c0) of the input in shared memory with asynchronous
+// 16-byte copies (all of a thread's copies in flight at once, no registers
+// held); a warp moves one 512-byte input row segment per step and elements
+// outside the input are zero-filled.  Ends with the copies complete and the
+// tile visible to the whole CTA.
 __device__ __forceinline__ void stage_tile(const QuantParams& p, uint32_t (&tile)[kColTileRows][kColTileCols / 2],
                                            int64_t r0, int64_t c0) {
   const int tid = threadIdx.x;
-#pragma unroll 4
+#pragma unroll
   for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
     const int idx = k * kColThreads + tid;
     const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r0 + row < p.rows && c0 + vec * 8 < p.cols) val = ldg_nc(p.x + (r0 + row) * p.ld + c0 + vec * 8);
-    *reinterpret_cast<uint4*>(&tile[row][vec * 4]) = val;
+    const bool ok = r0 + row < p.rows && c0 + vec * 8 < p.cols;
+    const uint16_t* src = ok ? p.x + (r0 + row) * p.ld + c0 + vec * 8 : p.x;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(&tile[row][vec * 4])), "l"(src),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
 }
 
 // Column-wise (transposed) quantisation of a staged tile.  Output row c =
@@ -481,7 +488,6 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) 
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
     stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);
-    __syncthreads();
     cols_tile<kSR, kRHT, kTwoD, kMMA>(p, tile, tr * kColTileRows, tc * kColTileCols, sg, den);
     __syncthreads();
   }
@@ -541,7 +547,6 @@ __global__ void __launch_bounds__(kColThreads) quant_dual_kernel(QuantParams pr,
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
     const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
     stage_tile(pr, tile, r0, c0);
-    __syncthreads();
     rows_tile<kRowSR, kMMA>(pr, tile, r0, c0, sg_r, den_r);
     cols_tile<true, true, false, kMMA>(pc, tile, r0, c0, sg_c, den_c);
     __syncthreads();
