@@ -88,6 +88,11 @@ def lib():
         L.o_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                  ctypes.c_uint32, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.o_mx_block_exponent.restype = ctypes.c_int
+        L.o_mx_block_exponent.argtypes = [ctypes.c_float]
+        L.o_quantize_mx.restype = ctypes.c_int
+        L.o_quantize_mx.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_void_p]
         L.o_gemm.restype = None
         L.o_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
@@ -236,6 +241,36 @@ def quantize(x_bf16_bits: np.ndarray, flags: int = 0, rht_seed: int = 0, sr_seed
     if rc != 0:
         raise ValueError(f"oracle cannot block shape {x.shape} with flags {flags:#x}")
     return QTensor(codes, scales, float(amax[0]), float(sg[0]))
+
+
+# ------------------------------------------------------------------ MXFP4 --
+def mx_block_exponent(amax_b: float) -> int:
+    return int(lib().o_mx_block_exponent(ctypes.c_float(amax_b)))
+
+
+def quantize_mx(x_bf16_bits: np.ndarray):
+    """MXFP4 of a 2-D bf16 array (uint16 patterns): (codes [rows, cols/2],
+    E8M0 scales [rows, cols/32])."""
+    x = np.ascontiguousarray(np.asarray(x_bf16_bits))
+    if x.dtype != np.uint16:
+        raise TypeError("pass bf16 bit patterns as uint16")
+    rows, cols = x.shape
+    codes = np.empty((rows, cols // 2), np.uint8)
+    scales = np.empty((rows, cols // 32), np.uint8)
+    if lib().o_quantize_mx(_ptr(x), rows, cols, cols, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError(f"MXFP4 needs cols % 32 == 0, got {x.shape}")
+    return codes, scales
+
+
+def dequantize_mx(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """fp64 values of an MXFP4 operand: E2M1 value times 2^(byte - 127)."""
+    rows = codes.shape[0]
+    tab = e2m1_table()
+    lo, hi = codes & 0xF, codes >> 4
+    v = np.empty((rows, codes.shape[1] * 2), np.float64)
+    v[:, 0::2] = tab[lo]
+    v[:, 1::2] = tab[hi]
+    return v * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
 
 
 # ------------------------------------------------------------------- GEMM --

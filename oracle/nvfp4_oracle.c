@@ -300,6 +300,55 @@ int o_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
   return 0;
 }
 
+/* --------------------------------------------------------------- MXFP4 --- */
+
+/* MXFP4, the power-of-two-scaled open format the pages set NVFP4 against
+ * ([P3] section "Cos'è NVFP4 ...", second paragraph: NVFP4 has much less
+ * error than power-of-two solutions such as MXFP4; [P4] section
+ * "Сравнительный ландшафт низкоразрядных форматов": NVFP4 uses smaller
+ * quantisation blocks and exact scale factors than the open MXFP4 standard).
+ * The pages give no further detail; the reading (the open microscaling
+ * layout): 32 consecutive elements of a row share one scale 2^e stored as an
+ * E8M0 biased exponent (byte = e + 127), e = floor(log2(amax_b)) - 2 so that
+ * the block amax lies in [4, 8) * 2^e, clamped to [-127, 127], and e = -127
+ * for an all-zero block; elements are E2M1 round-to-nearest-even of x / 2^e,
+ * saturating at 6, sign kept.  No tensor-level scale. */
+int o_mx_block_exponent(float amax_b) {
+  if (!(amax_b > 0.0f)) return -127;
+  int ex = 0;
+  (void)frexp((double)amax_b, &ex);  /* amax_b = m * 2^ex, m in [0.5, 1) */
+  int e = (ex - 1) - 2;              /* floor(log2(amax_b)) - 2 */
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+int o_quantize_mx(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                  uint8_t* scales) {
+  if (cols % 32 != 0) return -1;
+  int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      float amax_b = 0.0f;
+      for (int j = 0; j < 32; ++j) amax_b = fmaxf(amax_b, fabsf(bf16_to_f32(x[r * ld + b * 32 + j])));
+      int e = o_mx_block_exponent(amax_b);
+      scales[r * nb + b] = (uint8_t)(e + 127);
+      for (int j = 0; j < 32; j += 2) {
+        uint8_t q[2];
+        for (int h = 0; h < 2; ++h) {
+          /* x / 2^e is exact in double and representable in float: the
+           * bf16 significand has 8 bits and |x / 2^e| < 8 */
+          double v = ldexp((double)bf16_to_f32(x[r * ld + b * 32 + j + h]), -e);
+          q[h] = o_e2m1_encode_rne((float)v);
+        }
+        codes[r * (cols / 2) + (b * 32 + j) / 2] = (uint8_t)(q[0] | (q[1] << 4));
+      }
+    }
+  }
+  return 0;
+}
+
 /* --------------------------------------------------------------- GEMM --- */
 
 /* Dequantised element k of row r: E2M1 value times its block's E4M3 scale;
