@@ -152,6 +152,26 @@ int nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, u
                         const float* amax_row_in, const float* amax_col_in, const nvfp4_tensor* out_row,
                         const nvfp4_tensor* out_col, nvfp4_stream_t stream);
 
+/* MXFP4 quantisation, for comparison with NVFP4: the power-of-two-scaled
+ * open format the pages set NVFP4 against ("NVFP4: cos'è e come supera FP8 e
+ * BF16 ...", section "Cos'è NVFP4 ...", second paragraph: NVFP4 has much less
+ * quantisation error than power-of-two solutions such as MXFP4; "FP4"
+ * (chaitex.ru/fp4), section "Сравнительный ландшафт низкоразрядных
+ * форматов": NVFP4 uses smaller blocks and exact scale factors).  Format
+ * (the open microscaling layout; the pages give no detail): 32 consecutive
+ * elements of a row share the scale 2^e, e = floor(log2(block amax)) - 2
+ * clamped to [-127, 127] (-127 for a zero or subnormal block maximum), stored
+ * as the E8M0 byte e + 127; elements are E2M1, round-to-nearest-even of
+ * x / 2^e saturating at 6, sign kept; no tensor scale.
+ *   x       bf16 [rows, cols], row stride ld elements (16-byte aligned,
+ *           ld % 8 == 0, cols % 32 == 0)
+ *   codes   [rows, cols/2] bytes, element 2j in the low nibble of byte j
+ *           (16-byte aligned)
+ *   scales  [rows, cols/32] E8M0 bytes, row-major
+ * Returns NVFP4_OK or a negative status code (nothing launched on error). */
+int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                         uint8_t* scales_e8m0, nvfp4_stream_t stream);
+
 /* Block-scaled NVFP4 GEMM, "TN": C[M, N] = s_gA * s_gB * A[M, K] * B[N, K]^T
  * with fp32 accumulation and a BF16 (round-to-nearest-even) result.
  * A and B must use NVFP4_SCALES_MMA, K = A->cols = B->cols, K % 256 == 0.

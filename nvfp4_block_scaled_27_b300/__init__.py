@@ -42,7 +42,8 @@ SCALES_CANONICAL = 0
 SCALES_MMA = 1
 
 EXPORTED = (
-    "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_quantize_dual", "nvfp4_gemm",
+    "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_quantize_dual", "nvfp4_quantize_mxfp4",
+    "nvfp4_gemm",
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3",
 )
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_quantize_rht_sr.argtypes = [vp, i64, i64, i64, u32, u64, u64, vp, tp, vp]
     L.nvfp4_quantize_dual.restype = ctypes.c_int
     L.nvfp4_quantize_dual.argtypes = [vp, i64, i64, i64, u32, u64, u64, u64, vp, vp, tp, tp, vp]
+    L.nvfp4_quantize_mxfp4.restype = ctypes.c_int
+    L.nvfp4_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp]
     L.nvfp4_gemm.restype = ctypes.c_int
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, vp]
     L.nvfp4_check_status.restype = ctypes.c_int
@@ -194,6 +197,24 @@ def nvfp4_quantize_dual(x: torch.Tensor, row_flags: int, row_sr_seed: int, rht_s
         None if amax_row_in is None else amax_row_in.data_ptr(), None if amax_col_in is None else amax_col_in.data_ptr(),
         ctypes.byref(cr), ctypes.byref(cc), _stream(stream))
     _check(rc, "nvfp4_quantize_dual")
+
+
+def nvfp4_quantize_mxfp4(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    _require_cuda(x, codes, scales)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise Nvfp4Error("x must be a 2-D bf16 tensor with unit column stride")
+    rc = load_library().nvfp4_quantize_mxfp4(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), codes.data_ptr(),
+                                             scales.data_ptr(), _stream(stream))
+    _check(rc, "nvfp4_quantize_mxfp4")
+
+
+def quantize_mxfp4(x: torch.Tensor, stream=None):
+    """MXFP4 codes [rows, cols/2] and E8M0 scales [rows, cols/32] of x."""
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, max(cols // 32, 0)), dtype=torch.uint8, device=x.device)
+    nvfp4_quantize_mxfp4(x, codes, scales, stream)
+    return codes, scales
 
 
 def nvfp4_gemm(a: NVFP4Tensor, b: NVFP4Tensor, c: torch.Tensor, stream=None) -> None:

@@ -177,6 +177,18 @@ int nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, u
                                      col_sr_seed, amax_row_in, amax_col_in, *out_row, *out_col, s);
 }
 
+int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes, uint8_t* scales_e8m0,
+                         nvfp4_stream_t stream) {
+  if (rows < 0 || cols < 0 || ld < cols || cols % 32 != 0 || ld % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (rows * (cols / 32)) >= (int64_t)1 << 31) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  int rc = check_device(&dev);
+  if (rc) return rc;
+  if (rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || !codes || !scales_e8m0 || !aligned16(x) || !aligned16(codes)) return NVFP4_ERR_INVALID_ARG;
+  return nvfp4::quantize_mx_launch(*dev, x, rows, cols, ld, codes, scales_e8m0, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc, nvfp4_stream_t stream) {
   int rc = check_tensor_buffers(A);
   if (rc) return rc;

@@ -32,6 +32,10 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
                          const float* amax_row_in, const float* amax_col_in, const nvfp4_tensor& out_row,
                          const nvfp4_tensor& out_col, cudaStream_t stream);
 
+// MXFP4 quantiser entry (arguments validated by the caller).
+int quantize_mx_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                       uint8_t* scales, cudaStream_t stream);
+
 // GEMM entry (arguments validated by the caller).
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
                 int64_t ldc, cudaStream_t stream);

@@ -692,6 +692,41 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- MXFP4 --
+// The power-of-two-scaled open format NVFP4 is compared with: 32-element row
+// blocks, scale 2^e with e = floor(log2(amax_b)) - 2 (clamped to
+// [-127, 127]; -127 for zero and subnormal block maxima) stored as the E8M0
+// byte e + 127, elements E2M1 round-to-nearest-even of x * 2^-e (exact),
+// saturating at 6.  One thread per block (four 16-byte loads).
+__global__ void __launch_bounds__(256) quant_mx_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                       int64_t ld, uint8_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales) {
+  const uint32_t nb = (uint32_t)(cols / 32);
+  const uint32_t total = (uint32_t)(rows * nb);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t r = i / nb, b = i - r * nb;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)r * ld + (int64_t)b * 32);
+    const uint4 u0 = ldg_nc(src), u1 = ldg_nc(src + 1), u2 = ldg_nc(src + 2), u3 = ldg_nc(src + 3);
+    const uint32_t mbits = pairs_to_f32_bits(absmax_pairs(absmax_pairs(absmax_pairs(absmax_pairs(0u, u0), u1), u2), u3));
+    const int ef = (int)((mbits >> 23) & 0xFFu);
+    const int e = (ef == 0) ? -127 : min(ef - 127 - 2, 127);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal float for e in [-127, 125]
+    float v0[16], v1[16];
+    unpack16(u0, u1, v0);
+    unpack16(u2, u3, v1);
+    const uint2 q0 = encode16_rne(v0, inv), q1 = encode16_rne(v1, inv);
+    *reinterpret_cast<uint4*>(codes + (int64_t)r * (cols / 2) + (int64_t)b * 16) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+    scales[(int64_t)r * nb + b] = (uint8_t)(e + 127);
+  }
+}
+
+int quantize_mx_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                       uint8_t* scales, cudaStream_t stream) {
+  quant_mx_kernel<<<grid_for(quant_mx_kernel, dev, rows * (cols / 32), 256), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(x), rows, cols, ld, codes, scales);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 // Dual-orientation quantisation (row-wise 1D + transposed RHT/SR).
 int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
                          bool row_sr, uint64_t row_sr_seed, uint64_t rht_seed, uint64_t col_sr_seed,
