@@ -80,7 +80,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int SF_COLS_PER_STAGE = KSTEPS * 4 + KSTEPS * 8;  // 48
 constexpr int EPI_BOX = 32;                                  // 32 x 32 BF16 store boxes
 constexpr int EPI_BUF_BYTES = EPI_BOX * EPI_BOX * 2;         // 2 KiB
-constexpr int TILE_GROUP = 8;                                // pair tiles along M per raster group
+constexpr int TILE_GROUP = 16;                               // pair tiles along M per raster group
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr int OFF_A = 0;
