@@ -84,6 +84,31 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_gemm(ctypes.byref(b), ctypes.byref(b), 16, 64, None) == nv.ERR_INVALID_ARG
 
 
+def test_dual_and_mxfp4_arguments_rejected_on_host(lib):
+    row = nv.CTensor(1, 1, 1, 1, 64, 256, nv.SCALES_MMA, 0)
+    col = nv.CTensor(1, 1, 1, 1, 256, 64, nv.SCALES_MMA, 0)
+    ok_args = (16, 64, 256, 256)
+    # 2D blocks / transposition are not row modes of the dual call
+    assert lib.nvfp4_quantize_dual(*ok_args, nv.BLOCK_2D, 0, 0, 0, None, None, ctypes.byref(row), ctypes.byref(col),
+                                   None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_dual(*ok_args, nv.TRANSPOSE_OUT, 0, 0, 0, None, None, ctypes.byref(row),
+                                   ctypes.byref(col), None) == nv.ERR_INVALID_ARG
+    # output shapes swapped, mixed scale layouts, rows % 64 for the MMA layout
+    assert lib.nvfp4_quantize_dual(*ok_args, 0, 0, 0, 0, None, None, ctypes.byref(col), ctypes.byref(row), None) \
+        == nv.ERR_INVALID_ARG
+    col_c = nv.CTensor(1, 1, 1, 1, 256, 64, nv.SCALES_CANONICAL, 0)
+    assert lib.nvfp4_quantize_dual(*ok_args, 0, 0, 0, 0, None, None, ctypes.byref(row), ctypes.byref(col_c), None) \
+        == nv.ERR_INVALID_ARG
+    row48 = nv.CTensor(1, 1, 1, 1, 48, 256, nv.SCALES_MMA, 0)
+    col48 = nv.CTensor(1, 1, 1, 1, 256, 48, nv.SCALES_MMA, 0)
+    assert lib.nvfp4_quantize_dual(16, 48, 256, 256, 0, 0, 0, 0, None, None, ctypes.byref(row48), ctypes.byref(col48),
+                                   None) == nv.ERR_INVALID_ARG
+    # MXFP4: cols % 32, ld < cols, ld % 8
+    assert lib.nvfp4_quantize_mxfp4(16, 4, 48, 48, 16, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_mxfp4(16, 4, 64, 32, 16, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_mxfp4(16, 4, 64, 68, 16, 16, None) == nv.ERR_INVALID_ARG
+
+
 def test_compute_calls_refuse_cpu_tensors():
     import torch
     x = torch.zeros(16, 16, dtype=torch.bfloat16)
