@@ -57,6 +57,25 @@ def _peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def reduce_step_time(ms: float, world: int) -> float:
+    """Length of the timed region for the whole job: the maximum over ranks
+    (every rank's steps have ended by then).  Works with the NCCL backend
+    (CUDA tensor) and with gloo (CPU tensor)."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank runs one replica of the step (weak
+    scaling), so the job does world x the per-rank work per step."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during a region."""
 
@@ -216,11 +235,7 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     nv.check_status(stream)
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_step_time(t0.elapsed_time(t1), world)
     ms_step = ms / args.steps
 
     gemm_ms = {n: statistics.mean(gemm_ev[k][i][0].elapsed_time(gemm_ev[k][i][1]) for k in range(args.steps))
@@ -238,7 +253,7 @@ def run_ours(args):
     fp4_sust = peaks["bf16_tflops_sustained"] * (13.5 / 2.25)
     traffic = _committed_traffic()
 
-    value = world * STEP_FLOPS / (ms_step * 1e-3) / 1e12
+    value = job_tflops(STEP_FLOPS, ms_step, world)
     e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
     context = cublas_context(device) if (rank == 0 and not args.no_context) else None
