@@ -253,33 +253,6 @@ __device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, ui
   return make_uint2(w[0], w[1]);
 }
 
-// 8 values -> one 32-bit word of codes (element 2j in the low nibble of
-// byte j), round-to-nearest-even.
-__device__ __forceinline__ uint32_t encode8_rne(const float (&v)[8], float enc) {
-  uint32_t w = 0u;
-#pragma unroll
-  for (int j = 0; j < 8; j += 2) {
-    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
-    uint32_t byte = e2m1x2_rne_mag(fabsf(s0), fabsf(s1));
-    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
-    w |= byte << (4 * j);
-  }
-  return w;
-}
-
-// 8 values with stochastic rounding; q0 is the pair index of element 0 and
-// hk = mix32(key ^ hi32(q0)) (the 4 pairs share hi32).
-__device__ __forceinline__ uint32_t encode8_sr(const float (&v)[8], float enc, uint32_t hk, uint64_t q0) {
-  uint32_t w = 0u;
-#pragma unroll
-  for (int j = 0; j < 8; j += 2) {
-    const uint32_t r = sr_word(hk, q0 + (uint64_t)(j / 2));
-    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
-    w += sr_pair_codes(s0, s1, r) << (4 * j);
-  }
-  return w;
-}
-
 // Offset of scale (row r, block kb) in the MMA layout (cols/64 atoms per
 // 128-row band, 512 bytes per atom).
 __host__ __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t atoms_per_band) {

@@ -292,65 +292,6 @@ __global__ void __launch_bounds__(256) quant_rows_1d_kernel(QuantParams p) {
   }
 }
 
-// ------------------------------------------------------- row-wise, 2D --
-// A warp owns a 16-row x 256-column strip (sixteen 16x16 tiles); lane l holds
-// columns [8 l, 8 l + 8) of all 16 rows (one 16-byte load per row, 512
-// contiguous bytes per warp load).  Lanes 2t and 2t + 1 share tile t: the
-// integer tile amax (exact for bf16) is combined with one shuffle, and the
-// tile's scale is written on each of its 16 rows.
-template <bool kSR, bool kMMA>
-__global__ void __launch_bounds__(256) quant_rows_2d_kernel(QuantParams p) {
-  float amax;
-  const float sg = tensor_scale(p, amax);
-  const float den = __fmul_rn(sg, 6.0f);
-  const int lane = threadIdx.x & 31;
-  const uint32_t nb = (uint32_t)(p.ocols / 16);            // 16-column blocks per row
-  const uint32_t strips = (uint32_t)((p.ocols + 255) / 256);
-  const uint32_t total = (uint32_t)(p.orows / 16) * strips;  // warp work items
-  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
-  for (uint32_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += warps) {
-    const uint32_t band = w / strips, strip = w - band * strips;
-    const int64_t col = (int64_t)strip * 256 + 8 * lane;  // first of this lane's 8 columns
-    const bool active = col < p.ocols;                    // cols % 16 == 0: pairs are both in or out
-    const uint16_t* base = p.x + (int64_t)band * 16 * p.ld + col;
-    uint4 u[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) u[r] = active ? ldg_nc(base + (int64_t)r * p.ld) : make_uint4(0u, 0u, 0u, 0u);
-    uint32_t m = 0u;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) m = absmax_pairs(m, u[r]);
-    m = pairs_to_f32_bits(m);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    if (!active) continue;
-    const uint32_t sc = block_scale_code(__uint_as_float(m), den);
-    const float enc = block_enc(sg, sc);
-    const uint32_t kb = (uint32_t)(col / 16);
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int64_t orow = (int64_t)band * 16 + r;
-      float v[8];
-      const uint32_t wd[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = bf16_lo(wd[i]);
-        v[2 * i + 1] = bf16_hi(wd[i]);
-      }
-      uint32_t q;
-      if (kSR) {
-        const uint64_t q0 = ((uint64_t)orow * (uint64_t)p.ocols + (uint64_t)col) >> 1;  // 4 pairs
-        q = encode8_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
-      } else {
-        q = encode8_rne(v, enc);
-      }
-      *reinterpret_cast<uint32_t*>(p.codes + orow * (p.ocols / 2) + col / 2) = q;
-      if ((lane & 1) == 0) {
-        const int64_t off = kMMA ? mma_scale_offset(orow, kb, nb / 4) : orow * nb + kb;
-        p.scales[off] = (uint8_t)sc;
-      }
-    }
-  }
-}
-
 // ------------------------------------------------- column-wise (x^T) --
 constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
 constexpr int kColTileCols = 256;  // input columns per tile
@@ -531,6 +472,68 @@ __device__ __forceinline__ void rows_tile(const QuantParams& p, const uint32_t (
   }
 }
 
+// Row-wise 2D (16x16 tile) quantisation of a staged tile: threads 2u and
+// 2u + 1 own the 16x16 tile u (tile row u / 16, tile column u % 16), eight
+// rows each; the integer tile amax (exact for bf16) is combined with one
+// shuffle, then each row is re-read from shared memory and encoded, and the
+// tile's scale is written on each of its 16 rows.  16 threads write 128
+// contiguous code bytes of a row.
+template <bool kSR, bool kMMA>
+__device__ __forceinline__ void rows2d_tile(const QuantParams& p,
+                                            const uint32_t (&tile)[kColTileRows][kColTileCols / 2], int64_t r0,
+                                            int64_t c0, float sg, float den) {
+  const int tid = threadIdx.x;
+  const int h = tid & 1, tcol = (tid >> 1) & 15, trow = tid >> 5;
+  const int64_t col = c0 + 16 * tcol;
+  const int lr0 = 16 * trow + 8 * h;  // first of this thread's 8 rows in the tile
+  uint32_t m = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 a = *reinterpret_cast<const uint4*>(&tile[lr0 + i][8 * tcol]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&tile[lr0 + i][8 * tcol + 4]);
+    m = absmax_pairs(absmax_pairs(m, a), b);
+  }
+  m = pairs_to_f32_bits(m);
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  if (col >= p.cols || r0 + 16 * trow >= p.rows) return;  // whole 16x16 tiles only (rows, cols % 16 == 0)
+  const uint32_t sc = block_scale_code(__uint_as_float(m), den);
+  const float enc = block_enc(sg, sc);
+  const int64_t nb = p.cols / 16, kb = col / 16;
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const int64_t r = r0 + lr0 + i;
+    const uint4 a = *reinterpret_cast<const uint4*>(&tile[lr0 + i][8 * tcol]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&tile[lr0 + i][8 * tcol + 4]);
+    float v[16];
+    unpack16(a, b, v);
+    uint2 q;
+    if (kSR) {
+      const uint64_t q0 = ((uint64_t)r * (uint64_t)p.cols + (uint64_t)col) >> 1;
+      q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+    } else {
+      q = encode16_rne(v, enc);
+    }
+    *reinterpret_cast<uint2*>(p.codes + r * (p.cols / 2) + col / 2) = q;
+    p.scales[kMMA ? mma_scale_offset(r, kb, nb / 4) : r * nb + kb] = (uint8_t)sc;
+  }
+}
+
+template <bool kSR, bool kMMA>
+__global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams p) {
+  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  float amax;
+  const float sg = tensor_scale(p, amax);
+  const float den = __fmul_rn(sg, 6.0f);
+  const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);
+    rows2d_tile<kSR, kMMA>(p, tile, tr * kColTileRows, tc * kColTileCols, sg, den);
+    __syncthreads();
+  }
+}
+
 // Dual-orientation quantisation: one read of each input tile produces the
 // row-wise 1D operand (pr: RNE or SR) and the transposed RHT + SR operand
 // (pc).  Results are bit-identical to the two separate kernels.
@@ -592,13 +595,14 @@ static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma
 
 template <bool kSR>
 static void launch_rows_2d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
-  const int64_t items = (p.orows / 16) * ((p.ocols + 255) / 256) * 32;  // one warp per strip
+  const int64_t tiles =
+      ((p.rows + kColTileRows - 1) / kColTileRows) * ((p.cols + kColTileCols - 1) / kColTileCols);
   if (mma) {
     auto k = quant_rows_2d_kernel<kSR, true>;
-    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
   } else {
     auto k = quant_rows_2d_kernel<kSR, false>;
-    k<<<grid_for(k, dev, items, 256), 256, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
   }
 }
 
