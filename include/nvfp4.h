@@ -192,6 +192,16 @@ const char* nvfp4_status_string(int status);
 /* Library version (major * 10000 + minor * 100 + patch). */
 int nvfp4_version(void);
 
+/* ---- failure-detection self-test ------------------------------------------ */
+/* Launch a one-warp kernel whose bounded mbarrier waits (the same two wait
+ * helpers every kernel of the library uses) wait on a barrier that nothing
+ * completes: after limit_us microseconds (1 .. 2,000,000) each wait gives up,
+ * raises the timeout bit of the device status word, and the kernel exits.
+ * The next nvfp4_check_status() returns NVFP4_ERR_TIMEOUT and the context
+ * stays usable.  This is how a lost arrival inside a kernel surfaces; no
+ * kernel traps or spins without a limit.  Not part of the pages' method. */
+int nvfp4_selftest_wait_timeout(uint32_t limit_us, nvfp4_stream_t stream);
+
 /* ---- codec diagnostics (exhaustive conversion checks) -------------------- */
 /* out[i] = E2M1 code (low nibble) of v[i] with round-to-nearest-even,
  * saturating, sign kept -- the element encoder the quantiser uses.

@@ -45,7 +45,7 @@ EXPORTED = (
     "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_quantize_dual", "nvfp4_quantize_mxfp4",
     "nvfp4_gemm",
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
-    "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3",
+    "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3", "nvfp4_selftest_wait_timeout",
 )
 
 
@@ -98,6 +98,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_version.restype = ctypes.c_int
     L.nvfp4_version.argtypes = []
+    L.nvfp4_selftest_wait_timeout.restype = ctypes.c_int
+    L.nvfp4_selftest_wait_timeout.argtypes = [u32, vp]
     L.nvfp4_encode_e2m1_rne.restype = ctypes.c_int
     L.nvfp4_encode_e2m1_rne.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e2m1_sr.restype = ctypes.c_int
@@ -229,6 +231,10 @@ def nvfp4_gemm(a: NVFP4Tensor, b: NVFP4Tensor, c: torch.Tensor, stream=None) -> 
 
 def nvfp4_check_status(stream=None) -> int:
     return int(load_library().nvfp4_check_status(_stream(stream)))
+
+
+def nvfp4_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(load_library().nvfp4_selftest_wait_timeout(limit_us, _stream(stream)), "nvfp4_selftest_wait_timeout")
 
 
 def nvfp4_encode_e2m1_rne(v: torch.Tensor, out: torch.Tensor, stream=None) -> None:

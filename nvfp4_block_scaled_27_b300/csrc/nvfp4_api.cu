@@ -247,6 +247,14 @@ const char* nvfp4_status_string(int status) {
 
 int nvfp4_version(void) { return 100; }
 
+int nvfp4_selftest_wait_timeout(uint32_t limit_us, nvfp4_stream_t stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  int rc = check_device(&dev);
+  if (rc) return rc;
+  return nvfp4::selftest_wait_launch(*dev, (uint64_t)limit_us * 1000ull, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int nvfp4_encode_e2m1_rne(const float* v, int64_t n, uint8_t* out, nvfp4_stream_t stream) {
   if (n < 0 || (n > 0 && (!v || !out))) return NVFP4_ERR_INVALID_ARG;
   if (n == 0) return NVFP4_OK;

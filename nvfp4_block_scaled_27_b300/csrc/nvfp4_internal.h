@@ -40,6 +40,9 @@ int quantize_mx_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
                 int64_t ldc, cudaStream_t stream);
 
+// Bounded-wait self-test.
+int selftest_wait_launch(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
+
 // Codec diagnostics.
 int encode_e2m1_rne_launch(const float* v, int64_t n, uint8_t* out, cudaStream_t stream);
 int encode_e2m1_sr_launch(const float* v, const uint16_t* u, int64_t n, uint8_t* out,

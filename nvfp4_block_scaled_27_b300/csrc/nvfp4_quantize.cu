@@ -814,6 +814,27 @@ __global__ void encode_e4m3_kernel(const float* t, int64_t n, uint8_t* out) {
   }
 }
 
+// Self-test of the bounded waits: one warp waits, with both helpers the
+// kernels use (the C++ spin and the single-asm-block spin), on an mbarrier
+// that nothing arrives on; each gives up after limit_ns, raising the
+// timeout bit, and the kernel returns.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, status, limit_ns);
+  __syncwarp();
+  (void)mbar_wait_spin(smem_u32(&bar), 0, status, limit_ns);
+}
+
+int selftest_wait_launch(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, dev.status);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 static int diag_grid(int64_t n) {
   const int64_t g = (n + 255) / 256;
   return (int)(g < 1 ? 1 : (g > 65536 ? 65536 : g));

@@ -184,3 +184,19 @@ def test_sr_seeds_differ_and_repeat():
     c = nv.quantize(x, nv.ROUND_SR, sr_seed=2).codes.clone()
     assert torch.equal(a, b)
     assert not torch.equal(a, c)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A kernel whose bounded waits wait on a barrier nothing completes gives
+    up after the limit, the status word reports the timeout, and the next
+    calls run normally."""
+    assert nv.nvfp4_check_status() == nv.OK
+    nv.nvfp4_selftest_wait_timeout(20000)   # 20 ms per wait
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.ERR_TIMEOUT
+    assert nv.nvfp4_check_status() == nv.OK  # read-and-clear
+    x = make_bf16(TensorSpec(64, 256, 1.0), device="cuda")
+    q = nv.quantize(x)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.OK
+    assert_quant_equal(q, o.quantize(bf16_bits(x), 0), "after timeout")
