@@ -88,13 +88,6 @@ __host__ __device__ __forceinline__ uint32_t rht_sign_bits(uint64_t rht_seed) {
   return mix32(stream_key(rht_seed, kTagRHT)) & 0xFFFFu;
 }
 
-// Random bits for 16 consecutive output elements starting at index i0
-// (i0 % 16 == 0): one hash word per element pair; the even element takes
-// the low half-word.  hk = mix32(key ^ hi32(i0 >> 1)), shared by the pairs.
-__device__ __forceinline__ uint32_t sr_word(uint32_t hk, uint64_t pair_index) {
-  return mix32(hk ^ (uint32_t)pair_index);
-}
-
 // --------------------------------------------------------------- RHT-16 --
 // y = 1/4 * H16 * (d (.) x): sign flips, Walsh-Hadamard butterflies with
 // strides 1, 2, 4, 8 ((a, b) -> (a + b, a - b)), then the exact 1/4 scaling.
@@ -359,15 +352,6 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 2-D TMA tile load into shared memory, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
 // 2-D TMA tile load into this CTA's shared memory whose completion is
 // counted on an mbarrier given by its cluster address, which may lie in the
 // other CTA of the pair (CTA-pair form).
@@ -391,54 +375,12 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
 
-// ---- tcgen05 ----
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Arrive on an mbarrier once all previously issued tcgen05 async operations
-// of this thread (MMAs, copies) have completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// Copy a 32-row x 16-byte block of shared memory into tensor memory,
-// replicated into all four 32-lane sub-partitions.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// D (+)= (A * SFA) x (B * SFB)^T, NVFP4 operands from shared memory, E4M3
-// scales from tensor memory, fp32 accumulator in tensor memory.
-__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
