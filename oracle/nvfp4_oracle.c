@@ -37,7 +37,10 @@
  *   - SR random bits: 16 bits per element from the "lowbias32" integer hash
  *     (C. Wellons, hash-prospector, 2018, public domain) keyed by the seed and
  *     the element's row-major index in the OUTPUT orientation;
- *   - packing: the even column goes to the low nibble.
+ *   - packing: the even column goes to the low nibble;
+ *   - MXFP4 (the comparison format): 32-element row blocks, scale 2^e stored
+ *     as E8M0, e = floor(log2(block amax)) - 2 clamped to [-127, 127],
+ *     elements E2M1 round-to-nearest-even of x / 2^e.
  * Every fp32 operation below is a single IEEE round-to-nearest-even operation;
  * build with -ffp-contract=off so no multiply-add is fused.
  */
