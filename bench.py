@@ -427,7 +427,7 @@ def _oracle_sample(rows_a=8, cols_n=256):
     return flops, time.time() - t
 
 
-def cpu_baseline(args, rows_a=128, cols_n=512):
+def cpu_baseline(args, rows_a=256, cols_n=512):
     import oracle as o
     o.build()
     flops, secs = _oracle_sample(rows_a, cols_n)
