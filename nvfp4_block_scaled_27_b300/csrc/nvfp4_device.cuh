@@ -66,14 +66,15 @@ __device__ __forceinline__ uint32_t sign_nibble(float v) { return (__float_as_ui
 // ------------------------------------------------------------------ hash --
 // "lowbias32" 32-bit integer finaliser (C. Wellons, hash-prospector, 2018):
 // xorshift 16, *0x7feb352d, xorshift 15, *0x846ca68b, xorshift 16 (mod 2^32).
-__host__ __device__ __forceinline__ uint32_t mix32(uint32_t x) {
-  x ^= x >> 16;
+// mix32_tail is everything after the first xorshift.
+__host__ __device__ __forceinline__ uint32_t mix32_tail(uint32_t x) {
   x *= 0x7feb352du;
   x ^= x >> 15;
   x *= 0x846ca68bu;
   x ^= x >> 16;
   return x;
 }
+__host__ __device__ __forceinline__ uint32_t mix32(uint32_t x) { return mix32_tail(x ^ (x >> 16)); }
 
 // Key of a (64-bit seed, 32-bit stream tag) pair.
 __host__ __device__ __forceinline__ uint32_t stream_key(uint64_t seed, uint32_t tag) {
@@ -179,10 +180,12 @@ __device__ __forceinline__ float block_enc(float sg, uint32_t sc) {
 // Encode 16 values with a common factor into 8 bytes (two 32-bit words),
 // round-to-nearest-even.
 __device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
+  const uint64_t e2 = f2_pack(enc, enc);
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
-    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    float s0, s1;
+    f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), e2), s0, s1);
     uint32_t byte = e2m1x2_rne_mag(fabsf(s0), fabsf(s1));
     byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
     w[j / 8] |= byte << (8 * ((j / 2) % 4));
@@ -191,10 +194,15 @@ __device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
 }
 
 // Random words of the 8 pairs q0 .. q0 + 7 of a 16-element block (q0 a
-// multiple of 8, so the pairs share hi32 and hk).
+// multiple of 8, so the pairs share hi32 and hk).  w[j] = mix32(hk ^ (q0lo +
+// j)); since q0lo + j == q0lo ^ j and j < 8 leaves bits 16 and up unchanged,
+// the first xorshift is taken once for the block: mix32(g ^ j) ==
+// mix32_tail((g ^ (g >> 16)) ^ j) with g = hk ^ q0lo.
 __device__ __forceinline__ void sr_words8(uint32_t hk, uint32_t q0lo, uint32_t (&w)[8]) {
+  uint32_t g = hk ^ q0lo;
+  g ^= g >> 16;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j] = mix32(hk ^ (q0lo + (uint32_t)j));
+  for (int j = 0; j < 8; ++j) w[j] = mix32_tail(g ^ (uint32_t)j);
 }
 
 // SR codes (sign included) of two values s0, s1 (already scaled by the
@@ -237,10 +245,12 @@ __device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, ui
                                              uint64_t q0) {
   uint32_t r[8];
   sr_words8(hk, (uint32_t)q0, r);
+  const uint64_t e2 = f2_pack(enc, enc);
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
-    const float s0 = __fmul_rn(v[j], enc), s1 = __fmul_rn(v[j + 1], enc);
+    float s0, s1;
+    f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), e2), s0, s1);
     w[j / 8] += sr_pair_codes(s0, s1, r[j / 2]) << (8 * ((j / 2) % 4));
   }
   return make_uint2(w[0], w[1]);

@@ -336,9 +336,13 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
   // output row (two 16-byte stores) and one 32-bit word of four scales.
   const bool whole = (r0 + kColTileRows <= R) && ((R & 31) == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0);
-  uint2 qa[4], qb[4];
+  // Codes shift through four registers per output row, oldest chunk first,
+  // so the chunk loop needs no indexed arrays and can stay rolled (the
+  // unrolled body overflows the instruction cache).
+  uint2 qa0 = make_uint2(0u, 0u), qa1 = qa0, qa2 = qa0, qa3 = qa0;
+  uint2 qb0 = qa0, qb1 = qa0, qb2 = qa0, qb3 = qa0;
   uint32_t sca = 0u, scb = 0u;
-#pragma unroll
+#pragma unroll 1
   for (int k = 0; k < kColTileRows / 16; ++k) {
     const int64_t rb = r0 + 16 * k;  // first input row of the block
     if (rb >= R) break;              // uniform across the CTA
@@ -378,10 +382,10 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
       q0 = encode16_rne_scaled(v0);
       q1 = encode16_rne_scaled(v1);
     }
-    qa[k] = q0;
-    qb[k] = q1;
-    sca |= sc0 << (8 * k);
-    scb |= sc1 << (8 * k);
+    qa0 = qa1; qa1 = qa2; qa2 = qa3; qa3 = q0;
+    qb0 = qb1; qb1 = qb2; qb2 = qb3; qb3 = q1;
+    sca = (sca >> 8) | (sc0 << 24);
+    scb = (scb >> 8) | (sc1 << 24);
     if (!whole) {
       *reinterpret_cast<uint2*>(p.codes + c * (R / 2) + rb / 2) = q0;
       *reinterpret_cast<uint2*>(p.codes + (c + 1) * (R / 2) + rb / 2) = q1;
@@ -398,10 +402,10 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
   if (whole && col_ok) {
     uint8_t* o0 = p.codes + c * (R / 2) + r0 / 2;
     uint8_t* o1 = o0 + R / 2;
-    *reinterpret_cast<uint4*>(o0) = make_uint4(qa[0].x, qa[0].y, qa[1].x, qa[1].y);
-    *reinterpret_cast<uint4*>(o0 + 16) = make_uint4(qa[2].x, qa[2].y, qa[3].x, qa[3].y);
-    *reinterpret_cast<uint4*>(o1) = make_uint4(qb[0].x, qb[0].y, qb[1].x, qb[1].y);
-    *reinterpret_cast<uint4*>(o1 + 16) = make_uint4(qb[2].x, qb[2].y, qb[3].x, qb[3].y);
+    *reinterpret_cast<uint4*>(o0) = make_uint4(qa0.x, qa0.y, qa1.x, qa1.y);
+    *reinterpret_cast<uint4*>(o0 + 16) = make_uint4(qa2.x, qa2.y, qa3.x, qa3.y);
+    *reinterpret_cast<uint4*>(o1) = make_uint4(qb0.x, qb0.y, qb1.x, qb1.y);
+    *reinterpret_cast<uint4*>(o1 + 16) = make_uint4(qb2.x, qb2.y, qb3.x, qb3.y);
     const int64_t kb0 = r0 / 16;  // a multiple of 4: the four scales share one word
     if (kMMA) {
       *reinterpret_cast<uint32_t*>(p.scales + mma_scale_offset(c, kb0, kb_per_row / 4)) = sca;
@@ -537,8 +541,10 @@ __global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams 
 // Dual-orientation quantisation: one read of each input tile produces the
 // row-wise 1D operand (pr: RNE or SR) and the transposed RHT + SR operand
 // (pc).  Results are bit-identical to the two separate kernels.
+// Six CTAs per SM (80 registers, 6 x 32 KiB tiles): the encodes are bound
+// by instruction issue, and more resident warps hide their latencies.
 template <bool kRowSR, bool kMMA>
-__global__ void __launch_bounds__(kColThreads) quant_dual_kernel(QuantParams pr, QuantParams pc) {
+__global__ void __launch_bounds__(kColThreads, 6) quant_dual_kernel(QuantParams pr, QuantParams pc) {
   __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
   float amax_r, amax_c;
   const float sg_r = tensor_scale(pr, amax_r);
@@ -568,6 +574,11 @@ static int64_t resident_ctas(const void* kernel, int threads, const DeviceInfo& 
   auto it = m.find(kernel);
   if (it == m.end()) {
     int n = 0;
+    // Kernels that stage tiles in shared memory ask for the largest carveout
+    // so shared memory does not cap the CTAs per SM below the register limit.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.sharedSizeBytes > 0)
+      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
     it = m.emplace(kernel, n).first;
   }
