@@ -257,6 +257,8 @@ def run_ours(args):
     e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
     context = cublas_context(device) if (rank == 0 and not args.no_context) else None
+    if context is not None:
+        context["step_comparison"] = step_comparison(context, ms_step)
     clocks = clk.summary()
 
     if rank == 0:
@@ -555,6 +557,25 @@ def cublas_context(device):
         out[name] = res
         del a, b
     torch.cuda.empty_cache()
+    return out
+
+
+def step_comparison(context, ms_step):
+    """The step against the same three GEMMs run by cuBLAS(Lt) in BF16 and in
+    FP8 E4M3: the sum of the library GEMM times, and that sum divided by the
+    NVFP4 step time (quantisation included).  The BF16 sum is a whole BF16
+    step (nothing to quantise); the FP8 sum leaves out FP8's own casts, so
+    it flatters FP8.  None when a GEMM time is missing."""
+    if not context:
+        return None
+    out = {}
+    for kind in ("bf16", "fp8_e4m3"):
+        times = [context.get(n, {}).get(kind, {}).get("ms") for n in ("fprop", "dgrad", "wgrad")]
+        if any(t is None for t in times):
+            out[kind] = None
+            continue
+        total = sum(times)
+        out[kind] = {"gemms_ms": round(total, 4), "speedup_of_nvfp4_step": round(total / ms_step, 3)}
     return out
 
 
