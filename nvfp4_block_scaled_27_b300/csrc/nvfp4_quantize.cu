@@ -576,10 +576,18 @@ static int64_t resident_ctas(const void* kernel, int threads, const DeviceInfo& 
     int n = 0;
     // Kernels that stage tiles in shared memory ask for the largest carveout
     // so shared memory does not cap the CTAs per SM below the register limit.
+    // Both calls are hints: a failure falls back to one CTA per SM and its
+    // error is cleared, so the launch check that follows does not see it.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.sharedSizeBytes > 0)
-      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e == cudaSuccess && fa.sharedSizeBytes > 0)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
     it = m.emplace(kernel, n).first;
   }
   return (int64_t)it->second * dev.sm_count;
