@@ -522,10 +522,13 @@ def run_sweep(args):
 
 # ---------------------------------------------------- library context --
 def cublas_context(device):
-    """The same three GEMM shapes in BF16 (torch.matmul -> cuBLAS) and FP8
-    E4M3 (torch._scaled_mm -> cuBLASLt), CUDA-event timed: context for the
-    NVFP4 GEMMs, not a target.  Entries that the installed torch cannot run
-    are null."""
+    """The same three GEMM shapes in BF16 (torch.matmul -> cuBLAS), FP8
+    E4M3 (torch._scaled_mm -> cuBLASLt) and NVFP4 (torch's scaled_mm with
+    1x16 block + tensor scales -> cuBLASLt, fed this library's quantised
+    operands), CUDA-event timed: context for the NVFP4 GEMMs, not a target.
+    Entries that the installed torch cannot run say why."""
+    import nvfp4_block_scaled_27_b300 as nv
+
     shapes = {"fprop": (T, F2, H), "dgrad": (T, H, F), "wgrad": (F, H, T)}
     out = {}
     g = torch.Generator(device=device).manual_seed(0)
@@ -533,10 +536,20 @@ def cublas_context(device):
         a = torch.randn(M, K, generator=g, device=device, dtype=torch.bfloat16)
         b = torch.randn(N, K, generator=g, device=device, dtype=torch.bfloat16)
         res = {}
-        for kind in ("bf16", "fp8_e4m3"):
+        for kind in ("bf16", "fp8_e4m3", "nvfp4_cublaslt"):
             try:
                 if kind == "bf16":
                     fn = lambda: torch.matmul(a, b.t())
+                elif kind == "nvfp4_cublaslt":
+                    F_ = torch.nn.functional
+                    qa, qb = nv.quantize(a, nv.BLOCK_1D), nv.quantize(b, nv.BLOCK_2D)
+                    rec = [F_.ScalingType.BlockWise1x16, F_.ScalingType.TensorWise]
+                    sw = F_.SwizzleType.SWIZZLE_32_4_4
+                    a4 = qa.codes.view(torch.float4_e2m1fn_x2)
+                    b4 = qb.codes.view(torch.float4_e2m1fn_x2).t()
+                    sa = [qa.scales.view(torch.float8_e4m3fn), qa.global_scale]
+                    sb = [qb.scales.view(torch.float8_e4m3fn), qb.global_scale]
+                    fn = lambda: F_.scaled_mm(a4, b4, sa, rec, sb, rec, sw, sw, output_dtype=torch.bfloat16)
                 else:
                     a8 = a.to(torch.float8_e4m3fn)
                     b8 = b.to(torch.float8_e4m3fn)
@@ -553,7 +566,7 @@ def cublas_context(device):
                 ms = e0.elapsed_time(e1) / 5
                 res[kind] = {"ms": round(ms, 4), "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}
             except Exception as exc:  # noqa: BLE001 - context only
-                res[kind] = {"unavailable": type(exc).__name__}
+                res[kind] = {"unavailable": f"{type(exc).__name__}: {str(exc)[:160]}"}
         out[name] = res
         del a, b
     torch.cuda.empty_cache()
@@ -561,15 +574,16 @@ def cublas_context(device):
 
 
 def step_comparison(context, ms_step):
-    """The step against the same three GEMMs run by cuBLAS(Lt) in BF16 and in
-    FP8 E4M3: the sum of the library GEMM times, and that sum divided by the
-    NVFP4 step time (quantisation included).  The BF16 sum is a whole BF16
-    step (nothing to quantise); the FP8 sum leaves out FP8's own casts, so
-    it flatters FP8.  None when a GEMM time is missing."""
+    """The step against the same three GEMMs run by cuBLAS(Lt) in BF16, FP8
+    E4M3 and NVFP4: the sum of the library GEMM times, and that sum divided
+    by the NVFP4 step time (quantisation included).  The BF16 sum is a whole
+    BF16 step (nothing to quantise); the FP8 and NVFP4 sums leave out the
+    quantisation, so they flatter the library.  None when a GEMM time is
+    missing."""
     if not context:
         return None
     out = {}
-    for kind in ("bf16", "fp8_e4m3"):
+    for kind in ("bf16", "fp8_e4m3", "nvfp4_cublaslt"):
         times = [context.get(n, {}).get(kind, {}).get("ms") for n in ("fprop", "dgrad", "wgrad")]
         if any(t is None for t in times):
             out[kind] = None

@@ -13,6 +13,7 @@ def test_step_comparison_sums_and_ratios():
     got = bench.step_comparison(ctx, 4.5)
     assert got["bf16"] == {"gemms_ms": 9.0, "speedup_of_nvfp4_step": 2.0}
     assert got["fp8_e4m3"] == {"gemms_ms": 4.5, "speedup_of_nvfp4_step": 1.0}
+    assert got["nvfp4_cublaslt"] is None
 
 
 def test_step_comparison_missing_entries():

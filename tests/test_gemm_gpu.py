@@ -168,3 +168,41 @@ def test_empty_gemm():
     c = nv.gemm(qa, qb)
     torch.cuda.synchronize()
     assert c.shape == (0, 128)
+
+
+def _cublaslt_nvfp4(qa, qb):
+    """C = s_gA s_gB A B^T by cuBLASLt's NVFP4 GEMM (torch's scaled_mm with
+    1x16 E4M3 block scales in the 32x4x4 swizzle plus fp32 tensor scales),
+    fed this library's codes and scales as they are."""
+    F = torch.nn.functional
+    if not (hasattr(F, "scaled_mm") and hasattr(torch, "float4_e2m1fn_x2")):
+        pytest.skip("this torch has no NVFP4 scaled_mm")
+    rec = [F.ScalingType.BlockWise1x16, F.ScalingType.TensorWise]
+    sw = F.SwizzleType.SWIZZLE_32_4_4
+    try:
+        return F.scaled_mm(qa.codes.view(torch.float4_e2m1fn_x2), qb.codes.view(torch.float4_e2m1fn_x2).t(),
+                           [qa.scales.view(torch.float8_e4m3fn), qa.global_scale], rec,
+                           [qb.scales.view(torch.float8_e4m3fn), qb.global_scale], rec, sw, sw,
+                           output_dtype=torch.bfloat16)
+    except RuntimeError as exc:  # the library, not this package, lacks the kernel
+        pytest.skip(f"cuBLASLt NVFP4 GEMM unavailable: {str(exc)[:200]}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 384, 1024)])
+def test_layout_pinned_by_cublaslt(M, N, K):
+    """The codes (even element in the low nibble) and the MMA scale layout
+    are the published 1x16 NVFP4 operand format: cuBLASLt's NVFP4 GEMM, fed
+    this library's quantised operands unchanged, gives the oracle's product
+    of those operands within the GEMM tolerance, and so does this library's
+    GEMM."""
+    a = make_bf16(TensorSpec(M, K, 1.0, 0.01, 50.0, 21), device="cuda")
+    b = make_bf16(TensorSpec(N, K, 0.02, 0.0, 1.0, 22), device="cuda")
+    qa = nv.quantize(a, nv.BLOCK_1D)
+    qb = nv.quantize(b, nv.BLOCK_2D)
+    lib = _cublaslt_nvfp4(qa, qb)
+    ours = nv.gemm(qa, qb)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.OK
+    ref = o.gemm(host_qtensor(qa), host_qtensor(qb))
+    gemm_tolerance_check(lib.float().cpu().numpy().astype(np.float64), ref)
+    gemm_tolerance_check(ours.float().cpu().numpy().astype(np.float64), ref)
