@@ -18,9 +18,13 @@ Sources for each step are cited in the C file:
     gradients, NVFP4-in / BF16-out GEMMs.
 
 Parity pinning: every function here is checked by ``tests/test_oracle_pins.py``
-against facts fixed outside the oracle.  The stochastic-rounding hash itself is
-self-specified (the pages name none), so the bit stream is parity unpinned
-beyond its published definition and statistical checks.
+against facts fixed outside the oracle.  The stochastic-rounding hash is the
+published "lowbias32" finaliser, a bijection.  The pins run its inverse, which
+is written from the published steps: inverse(mix32(x)) == x.  Running the SR
+bit stream backwards through that inverse recovers the pair index, the seed
+and the stream tag that the definition puts in.  The pages name no generator,
+so the stream's layout is this build's own reading.  The inversion pins the
+oracle to that reading.
 """
 from __future__ import annotations
 

@@ -164,6 +164,58 @@ def test_hash_basic_properties():
     assert chi2 < 40.0  # 15 dof; p ~ 5e-4
 
 
+# The published "lowbias32" finaliser is a bijection: xorshift 16,
+# x 0x7feb352d, xorshift 15, x 0x846ca68b, xorshift 16 (mod 2^32).  Its
+# inverse runs the steps backwards: a xorshift by s >= 16 is its own inverse,
+# a xorshift by 15 is undone by x ^ (x >> 15) ^ (x >> 30), and each odd
+# multiplier by its inverse mod 2^32.  A wrong shift, constant or step in
+# the oracle breaks inverse(mix32(x)) == x.
+_M32 = 0xFFFFFFFF
+
+
+def _unmix32(y: int) -> int:
+    y ^= y >> 16
+    y = (y * pow(0x846ca68b, -1, 1 << 32)) & _M32
+    y ^= (y >> 15) ^ (y >> 30)
+    y = (y * pow(0x7feb352d, -1, 1 << 32)) & _M32
+    y ^= y >> 16
+    return y
+
+
+def test_hash_inverts_to_its_input():
+    rng = np.random.default_rng(17)
+    xs = [int(v) for v in rng.integers(0, 2 ** 32, 2000, dtype=np.uint64)] + [1, 2, 0xFFFFFFFF, 0x80000000]
+    for x in xs:
+        assert _unmix32(o.mix32(x)) == x
+        assert o.mix32(_unmix32(x)) == x
+
+
+def test_sr_bit_stream_inverts_to_its_seed_and_tag():
+    """Running the SR stream backwards through the inverse finaliser
+    recovers what the definition says went in: the pair index q = i >> 1
+    (element 2q in the low half-word, 2q + 1 in the high one), the split of q
+    into hi32 and lo32, the key of (seed, 0x5352) and that key's own seed
+    halves and tag."""
+    for seed in (0, 1000, 0x123456789ABCDEF0):
+        key = None
+        for q in (0, 1, 2, 77, 2 ** 20 + 5, 2 ** 32 - 1, 2 ** 32, 2 ** 33 + 9):
+            w = o.sr_bits(seed, 2 * q) | (o.sr_bits(seed, 2 * q + 1) << 16)
+            inner = _unmix32(w) ^ (q & _M32)          # = mix32(key ^ hi32(q))
+            k = _unmix32(inner) ^ (q >> 32)
+            assert key is None or k == key
+            key = k
+        assert key == o.stream_key(seed, 0x5352)
+        tag = _unmix32(_unmix32(key) ^ (seed & _M32)) ^ (seed >> 32)
+        assert tag == 0x5352
+
+
+def test_rht_key_inverts_to_its_tag():
+    for seed in (0, 7, 0xDEADBEEF12345678):
+        key = o.stream_key(seed, 0x5248)
+        assert _unmix32(_unmix32(key) ^ (seed & _M32)) ^ (seed >> 32) == 0x5248
+        assert o.rht_signs(seed) == o.mix32(key) & 0xFFFF
+
+
 def test_rht_matrix_is_scaled_sylvester_hadamard():
     H = scipy.linalg.hadamard(16).astype(np.float64)  # Sylvester order
     for seed in (0, 7, 123456789):
