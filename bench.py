@@ -392,38 +392,53 @@ def run_e2e(nv, step, stream, device, args):
 
 
 # --------------------------------------------------------------- oracle --
-def _oracle_sample(rows_a=8, cols_n=256):
-    """Oracle work for a bounded slice of the step: quantise `rows_a` token
-    rows and `cols_n` weight rows for each of the three GEMMs and evaluate
-    those rows x cols outputs in fp64.  Returns (flops of the slice, s)."""
+def _oracle_inputs(rows_a=8, cols_n=256):
+    """The bf16 operand slabs (as uint16 bit patterns) of a bounded slice of
+    the step: `rows_a` token rows and `cols_n` weight rows for each of the
+    three GEMMs, cut from the same seeded tensors the GPU step uses.  Made
+    before any timing, as the GPU step's inputs are resident before its
+    timed region."""
     import numpy as np
 
-    import oracle as o
     from workloads import LLAMA3_8B_X_BWD, TensorSpec, bf16_bits
 
     def slab(spec, rows):
         return bf16_bits(make_bf16(TensorSpec(rows, spec.cols, spec.std, spec.outlier_p, spec.outlier_factor,
                                               spec.seed), device="cpu"))
 
+    tok = 16 * rows_a  # wgrad contracts over a token slab of 16 * rows_a tokens
+    return {
+        "rows_a": rows_a, "cols_n": cols_n, "tok": tok,
+        "x": slab(LLAMA3_8B_FPROP.a, rows_a),
+        "w": slab(LLAMA3_8B_FPROP.b, cols_n),
+        "dy": slab(LLAMA3_8B_DY, rows_a),
+        # dgrad's B operand is W^T [H, F]: its first cols_n rows are W's first cols_n columns
+        "w2": np.ascontiguousarray(slab(LLAMA3_8B_W_BWD, F)[:, :cols_n]),
+        "dyt": slab(LLAMA3_8B_DY, tok)[:, :cols_n].copy(),
+        "xt": slab(LLAMA3_8B_X_BWD, tok)[:, :cols_n].copy(),
+    }
+
+
+def _oracle_sample(inp):
+    """Oracle work for one slice of the step: quantise the slabs of
+    `_oracle_inputs` as the step does and evaluate the rows_a x cols_n
+    outputs of fprop and dgrad and the cols_n x cols_n outputs of wgrad in
+    fp64.  Returns (flops of the slice, seconds)."""
+    import oracle as o
+
+    rows_a, cols_n, tok = inp["rows_a"], inp["cols_n"], inp["tok"]
     t = time.time()
     flops = 0.0
     # fprop slice: X rows x W rows, K = 4096
-    qa = o.quantize(slab(LLAMA3_8B_FPROP.a, rows_a), 0)
-    qb = o.quantize(slab(LLAMA3_8B_FPROP.b, cols_n), o.FLAG_BLOCK_2D)
-    o.gemm(qa, qb)
+    o.gemm(o.quantize(inp["x"], 0), o.quantize(inp["w"], o.FLAG_BLOCK_2D))
     flops += 2.0 * rows_a * cols_n * H
-    # dgrad slice: dY rows x W^T rows (W [F, H] -> W^T rows are H), K = F
-    qdy = o.quantize(slab(LLAMA3_8B_DY, rows_a), o.FLAG_SR, sr_seed=sr_seed(0))
-    w2 = slab(LLAMA3_8B_W_BWD, F)[:, :cols_n]
-    qw2t = o.quantize(np.ascontiguousarray(w2), o.FLAG_BLOCK_2D | o.FLAG_TRANSPOSE)
-    o.gemm(qdy, qw2t)
+    # dgrad slice: dY rows x W^T rows, K = F
+    o.gemm(o.quantize(inp["dy"], o.FLAG_SR, sr_seed=sr_seed(0)),
+           o.quantize(inp["w2"], o.FLAG_BLOCK_2D | o.FLAG_TRANSPOSE))
     flops += 2.0 * rows_a * cols_n * F
-    # wgrad slice: contraction over a token slab of 16 * rows_a tokens
-    tok = 16 * rows_a
-    qdyt = o.quantize(slab(LLAMA3_8B_DY, tok)[:, :cols_n].copy(), o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE,
-                      rht_seed=RHT_SEED, sr_seed=sr_seed(1))
-    qxt = o.quantize(slab(LLAMA3_8B_X_BWD, tok)[:, :cols_n].copy(), o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE,
-                     rht_seed=RHT_SEED, sr_seed=sr_seed(2))
+    # wgrad slice: dY^T and X^T over the token slab, RHT + SR
+    qdyt = o.quantize(inp["dyt"], o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE, rht_seed=RHT_SEED, sr_seed=sr_seed(1))
+    qxt = o.quantize(inp["xt"], o.FLAG_RHT | o.FLAG_SR | o.FLAG_TRANSPOSE, rht_seed=RHT_SEED, sr_seed=sr_seed(2))
     o.gemm(qdyt, qxt)
     flops += 2.0 * cols_n * cols_n * tok
     return flops, time.time() - t
@@ -432,11 +447,18 @@ def _oracle_sample(rows_a=8, cols_n=256):
 def cpu_baseline(args, rows_a=256, cols_n=512):
     import oracle as o
     o.build()
-    flops, secs = _oracle_sample(rows_a, cols_n)
+    flops, secs = _oracle_sample(_oracle_inputs(rows_a, cols_n))
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": o.get_threads(), "kind": "oracle",
             "sample": f"fprop/dgrad/wgrad slices: {rows_a} token rows x {cols_n} output columns each "
-                      f"(quantisation of those operand rows included), {secs:.1f} s",
+                      f"(quantisation of those operand rows included, input generation not), {secs:.1f} s",
             "seconds": round(secs, 2)}
+
+
+# Per-step sample of the reference arm: small enough that the default
+# 5 + 20 steps end within a minute or two on the host's cores.
+REF_ROWS, REF_COLS = 16, 256
+REF_SAMPLE = (f"{REF_ROWS} token rows x {REF_COLS} output columns per GEMM per step (inputs made once, "
+              f"before timing)")
 
 
 def run_reference(args):
@@ -446,22 +468,22 @@ def run_reference(args):
         return
     import oracle as o
     o.build()
+    inp = _oracle_inputs(REF_ROWS, REF_COLS)
     for _ in range(args.warmup):
-        _oracle_sample(2, 64)
-    t = time.time()
-    flops = 0.0
+        _oracle_sample(inp)
+    flops = secs = 0.0
     for _ in range(args.steps):
-        f, _ = _oracle_sample(2, 64)
+        f, dt = _oracle_sample(inp)
         flops += f
-    secs = time.time() - t
+        secs += dt
     v = flops / secs / 1e12
     line = {"impl": "reference", "metric": "NVFP4 GEMM TFLOP/s over an MLP fwd+bwd step (quantisation included)",
             "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp64 oracle over nvfp4 operands", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": "2 token rows x 64 output columns per GEMM per step"},
+            "config": {"workload": WORKLOAD, "sample": REF_SAMPLE},
             "cpu_baseline": {"kind": "oracle", "cores": o.get_threads(), "value": v, "unit": "TFLOP/s",
-                             "sample": "2 token rows x 64 output columns per GEMM per step"},
+                             "sample": REF_SAMPLE},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
