@@ -455,6 +455,63 @@ def test_rht_quantize_closed_form():
         assert np.array_equal(u[16 * i:16 * i + 16], exp)
 
 
+@pytest.mark.parametrize("c", [1.5, 0.8125, 3.0e-3])
+@pytest.mark.parametrize("transposed", [False, True])
+def test_rht_tensor_amax_is_taken_after_the_transform(c, transposed):
+    """With the transform, the tensor amax is max |1/4 H16 (d (.) x)|, not
+    max |x| (random Hadamard transform on the wgrad inputs before 4-bit
+    quantisation: readjensen.com NVFP4 training-recipe article, MLP data-flow
+    paragraph).  Chunks x = c (d (.) h_k) have raw amax c and transformed
+    amax exactly 4c (H h_k = 16 e_k), so no amax is passed in and the oracle
+    must find 4c itself; s_g is then fl32(4c / 2688)."""
+    H = scipy.linalg.hadamard(16)
+    s = o.rht_signs(7)
+    d = np.array([-1.0 if (s >> j) & 1 else 1.0 for j in range(16)])
+    c32 = float(np.float32(torch.tensor(c).to(torch.bfloat16).float()))
+    ks = (0, 3, 9, 15)
+    chunk_rows = [c32 * d * H[k] for k in ks]
+    x = _bf16_bits(np.concatenate(chunk_rows).tolist())[None, :]  # [1, 64]: four chunks along the row
+    flags = o.FLAG_RHT | o.FLAG_SR
+    if transposed:
+        x = np.ascontiguousarray(x.T)  # [64, 1]: the chunks run along the input's rows
+        flags |= o.FLAG_TRANSPOSE
+    q = o.quantize(x, flags, rht_seed=7, sr_seed=5)
+    assert q.amax == 4.0 * c32, f"amax {q.amax}: raw max|x| is {c32}, transformed {4.0 * c32}"
+    assert q.sg == float(np.float32(4.0 * c32) / np.float32(2688.0))
+    # each chunk's transformed block is 4c at index k and exact zeros
+    # elsewhere, and 4c is the tensor amax, so its scale is the saturating
+    # code and the element encodes as 6 (exactly representable: SR leaves it)
+    assert list(q.scales[0]) == [0x7E] * 4
+    u = _unpack(q.codes)[0]
+    for i, k in enumerate(ks):
+        exp = np.zeros(16, np.uint8)
+        exp[k] = 7
+        assert np.array_equal(u[16 * i:16 * i + 16], exp)
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_rht_tensor_amax_matches_fp64_hadamard_product(transposed):
+    """Random inputs on a coarse grid (multiples of 2^-6 below 4, so every
+    butterfly sum is exact in fp32): the oracle's tensor amax equals
+    max |1/4 H16 diag(d) x| over all 16-chunks along the quantisation axis,
+    evaluated in fp64 with scipy's Sylvester matrix."""
+    rng = np.random.default_rng(21)
+    R, C = 48, 64
+    vals = rng.integers(-255, 256, size=(R, C)).astype(np.float64) * 2.0 ** -6
+    x = _bf16_bits(vals.astype(np.float32).ravel().tolist()).reshape(R, C)
+    s = o.rht_signs(11)
+    d = np.array([-1.0 if (s >> j) & 1 else 1.0 for j in range(16)])
+    T = 0.25 * scipy.linalg.hadamard(16).astype(np.float64) @ np.diag(d)
+    oriented = vals.T if transposed else vals  # output orientation [orows, ocols]
+    chunks = oriented.reshape(oriented.shape[0], -1, 16)
+    expect = float(np.max(np.abs(chunks @ T.T)))
+    assert expect != float(np.max(np.abs(vals)))  # the transform changes the amax here
+    flags = o.FLAG_RHT | o.FLAG_SR | (o.FLAG_TRANSPOSE if transposed else 0)
+    q = o.quantize(x, flags, rht_seed=11, sr_seed=2)
+    assert q.amax == expect
+    assert q.sg == float(np.float32(expect) / np.float32(2688.0))
+
+
 # ------------------------------------------------------------------ GEMM ---
 def _qt(codes_unpacked, scales, sg):
     c = np.asarray(codes_unpacked, np.uint8)
