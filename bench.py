@@ -139,23 +139,28 @@ class MlpStep:
     operand for wgrad (same RHT seed for both).  W (gate+up) is quantised 2D
     for fprop, the down-projection W 2D and transposed for dgrad."""
 
-    def __init__(self, nv, device):
+    def __init__(self, nv, device, tokens=T, hidden=H, ffn=F, gate_up=F2):
+        from dataclasses import replace
         self.nv = nv
         self.dev = device
-        self.x = make_bf16(LLAMA3_8B_FPROP.a, device=device)   # [T, H]
-        self.w = make_bf16(LLAMA3_8B_FPROP.b, device=device)   # [F2, H]
-        self.dy = make_bf16(LLAMA3_8B_DY, device=device)       # [T, F]
-        self.w2 = make_bf16(LLAMA3_8B_W_BWD, device=device)    # [F, H]
+        t, h, f, f2 = tokens, hidden, ffn, gate_up
+        self.dims = (t, h, f, f2)
+        self.x = make_bf16(replace(LLAMA3_8B_FPROP.a, rows=t, cols=h), device=device)   # [T, H]
+        self.w = make_bf16(replace(LLAMA3_8B_FPROP.b, rows=f2, cols=h), device=device)  # [F2, H]
+        self.dy = make_bf16(replace(LLAMA3_8B_DY, rows=t, cols=f), device=device)       # [T, F]
+        self.w2 = make_bf16(replace(LLAMA3_8B_W_BWD, rows=f, cols=h), device=device)    # [F, H]
         e = nv.empty_nvfp4
-        self.qx = e(T, H, device=device)
-        self.qxt = e(H, T, device=device)
-        self.qw = e(F2, H, device=device)
-        self.qdy = e(T, F, device=device)
-        self.qdyt = e(F, T, device=device)
-        self.qw2t = e(H, F, device=device)
-        self.y = torch.empty(T, F2, dtype=torch.bfloat16, device=device)
-        self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
-        self.dw = torch.empty(F, H, dtype=torch.bfloat16, device=device)
+        self.qx = e(t, h, device=device)
+        self.qxt = e(h, t, device=device)
+        self.qw = e(f2, h, device=device)
+        self.qdy = e(t, f, device=device)
+        self.qdyt = e(f, t, device=device)
+        self.qw2t = e(h, f, device=device)
+        self.y = torch.empty(t, f2, dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty(t, h, dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty(f, h, dtype=torch.bfloat16, device=device)
+        self.quant_elems = [t * h, f2 * h, t * f, f * h]
+        self.gemm_flops = {"fprop": 2.0 * t * f2 * h, "dgrad": 2.0 * t * h * f, "wgrad": 2.0 * f * h * t}
         # kernels per step: 2 per quantisation call (amax pass + encode), 3 GEMMs
         self.launches_per_step = 4 * 2 + 3
 
@@ -189,7 +194,6 @@ class MlpStep:
         # wgrad
         g(2, self.qdyt, self.qxt, self.dw)
 
-    quant_elems = [T * H, F2 * H, T * F, F * H]
     quant_names = ["X dual (1D RNE + RHT/SR transposed)", "W 2D", "dY dual (1D SR + RHT/SR transposed)", "W^T 2D"]
     # algorithmic bytes per element: read 2 B; write 0.5625 B per output operand
     quant_bytes_per_elem = [2.0 + 2 * 0.5625, QUANT_BYTES_PER_ELEM, 2.0 + 2 * 0.5625, QUANT_BYTES_PER_ELEM]
@@ -251,17 +255,39 @@ def run_ours(args):
     peaks, peak_src = _peaks()
     fp4_burst = peaks["bf16_tflops"] * (13.5 / 2.25)
     fp4_sust = peaks["bf16_tflops_sustained"] * (13.5 / 2.25)
-    traffic = _committed_traffic()
+    traffic = _committed_json("gemm_fprop_traffic.json", "dram_bytes_per_launch")
+    clocks = clk.summary()
 
     value = job_tflops(STEP_FLOPS, ms_step, world)
+    probe = qroof = sweep = None
+    if rank == 0:
+        probe = mma_probe(nv, clocks)
+        qroof = quant_roofline(nv, step, stream, peaks, args)
+        sweep = sweep_point(nv, stream, peaks, args) if not args.no_sweep else None
     e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
     context = cublas_context(device) if (rank == 0 and not args.no_context) else None
     if context is not None:
         context["step_comparison"] = step_comparison(context, ms_step)
-    clocks = clk.summary()
 
     if rank == 0:
+        roofline = {"kernel": "nvfp4_gemm_kernel, Llama 3 8B MLP fprop launch (M=32768, N=28672, K=4096)",
+                    "bound": "tensor", "achieved": round(fprop_tflops, 1),
+                    "peak": round(fp4_burst, 1), "unit": "TFLOP/s",
+                    "frac": round(fprop_tflops / fp4_burst, 4),
+                    "peak_note": f"{peak_src} cuBLAS bf16 burst {peaks['bf16_tflops']} TFLOP/s x 6 (nominal dense "
+                                 f"fp4/bf16 ratio 13.5/2.25); the kernel is timed inside a step of "
+                                 f"{ms_step * args.steps:.0f} ms, a burst",
+                    "frac_of_sustained_bf16_x6": round(fprop_tflops / fp4_sust, 4),
+                    "frac_of_pages_15pf_dense_nvfp4": round(fprop_tflops / 15000.0, 4),
+                    "all_three_gemms_tflops": round(gemm_tflops, 1),
+                    "algorithmic_bytes": GEMM_FPROP_BYTES,
+                    "traffic": traffic}
+        if probe is not None:
+            roofline["tcgen05_probe"] = probe
+            if probe.get("tflops_at_step_clock"):
+                roofline["frac_of_probe_at_step_clock"] = round(fprop_tflops / probe["tflops_at_step_clock"], 4)
+            roofline["frac_of_probe_at_max_clock"] = round(fprop_tflops / probe["tflops_at_max_clock"], 4)
         line = {
             "metric": "NVFP4 GEMM TFLOP/s over an MLP fwd+bwd step (quantisation included)",
             "value": round(value, 2),
@@ -286,16 +312,10 @@ def run_ours(args):
                          for nm, n, bpe, t in zip(step.quant_names, step.quant_elems, step.quant_bytes_per_elem,
                                                   quant_ms)],
             "quantize_gbs_all": round(quant_gbs, 1),
-            "roofline": {"kernel": "nvfp4_gemm_kernel, Llama 3 8B MLP fprop launch (M=32768, N=28672, K=4096)",
-                         "bound": "tensor", "achieved": round(fprop_tflops, 1),
-                         "peak": round(fp4_sust, 1), "unit": "TFLOP/s",
-                         "frac": round(fprop_tflops / fp4_sust, 4),
-                         "peak_note": f"{peak_src} bf16 sustained {peaks['bf16_tflops_sustained']} x 6 (nominal "
-                                      f"fp4/bf16 ratio): the GEMM runs inside a seconds-long step",
-                         "frac_of_burst": round(fprop_tflops / fp4_burst, 4),
-                         "all_three_gemms_tflops": round(gemm_tflops, 1),
-                         "algorithmic_bytes": GEMM_FPROP_BYTES,
-                         "traffic": traffic},
+            "quantize_ms_all": round(sum(quant_ms), 4),
+            "roofline": roofline,
+            "quant_roofline": qroof,
+            "quant_sweep_2e30": sweep,
             "cpu_baseline": cpu,
             "library_context": context,
             "e2e": e2e,
@@ -307,17 +327,124 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def _committed_traffic():
-    """DRAM bytes (read + write) of one fprop GEMM launch, from the committed
-    ncu summary of that launch (null if absent)."""
-    path = os.path.join(ROOT, "profiles", "gemm_fprop_traffic.json")
+def _committed_json(name, key):
+    """A figure from a committed ncu summary under profiles/ (DRAM bytes of
+    one launch), or None if the summary is absent."""
+    path = os.path.join(ROOT, "profiles", name)
     if os.path.exists(path):
         try:
             with open(path) as f:
-                return json.load(f).get("dram_bytes_per_launch")
+                return json.load(f).get(key)
         except (OSError, ValueError):
             return None
     return None
+
+
+def _event_ms(fn, stream, reps, warmup=2, flush=None):
+    """Median CUDA-event time of fn() on `stream` (events on that stream)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        ev = []
+        for _ in range(reps):
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ev.append((e0, e1))
+    stream.synchronize()
+    t = sorted(a.elapsed_time(b) for a, b in ev)
+    return t[len(t) // 2]
+
+
+def mma_probe(nv, clocks):
+    """The FP4 tensor-core rate measured by the library's MMA-rate probe
+    (back-to-back pair MMAs, no memory traffic), scaled to the SM clocks:
+    the probe's own, the step's sampled median and the maximum."""
+    try:
+        r = nv.measure_mma_rate(8192, 256)
+    except Exception as exc:  # noqa: BLE001 - reported, not fatal
+        return {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
+    per_clk = r["flop_per_sm_per_cycle"] * r["sms"]
+    r["tflops_at_max_clock"] = round(per_clk * 2.032e9 / 1e12, 1)
+    if clocks.get("sm_mhz"):
+        r["tflops_at_step_clock"] = round(per_clk * clocks["sm_mhz"] * 1e6 / 1e12, 1)
+        r["step_clock_mhz"] = clocks["sm_mhz"]
+    return r
+
+
+def quant_roofline(nv, step, stream, peaks, args):
+    """Roofline of the dominant quantiser call, the dY dual call (32768 x
+    14336: row-wise 1D SR and transposed RHT + SR from one pass).  Algorithmic
+    bytes: read the bf16 input once (2 B/elem), write both operands' codes and
+    scales (2 x 0.5625 B/elem).  Timed twice: the whole call (amax pass +
+    encode kernel) and the encode kernel alone (both amaxes supplied, so the
+    call launches only quant_dual_kernel).  dY is larger than L2."""
+    nv_ = nv
+    t, h, f, f2 = step.dims
+    n = t * f
+    alg = n * (2.0 + 2 * 0.5625)
+    amax_r = step.qdy.amax.clone()
+    amax_c = step.qdyt.amax.clone()
+    reps = max(5, min(args.steps, 20))
+    call = lambda: nv_.nvfp4_quantize_dual(step.dy, nv_.ROUND_SR, sr_seed(0), RHT_SEED, sr_seed(1), None, None,  # noqa
+                                           step.qdy, step.qdyt, stream)
+    enc = lambda: nv_.nvfp4_quantize_dual(step.dy, nv_.ROUND_SR, sr_seed(0), RHT_SEED, sr_seed(1), amax_r, amax_c,  # noqa
+                                          step.qdy, step.qdyt, stream)
+    torch.cuda.synchronize()
+    ms_call = _event_ms(call, stream, reps)
+    ms_enc = _event_ms(enc, stream, reps)
+    nv_.check_status(stream)
+    hbm = peaks["hbm_gbs"]
+    a_call = alg / (ms_call * 1e-3) / 1e9
+    a_enc = alg / (ms_enc * 1e-3) / 1e9
+    return {"kernel": "quant_dual_kernel<1,1>: dY [32768, 14336] -> row-wise 1D SR + transposed RHT/SR operands",
+            "bound": "hbm", "unit": "GB/s", "peak": hbm, "peak_note": "measured HBM copy bandwidth (MEASURED_PEAKS)",
+            "algorithmic_bytes": int(alg), "bytes_per_elem": 3.125,
+            "achieved": round(a_enc, 1), "frac": round(a_enc / hbm, 4), "encode_ms": round(ms_enc, 4),
+            "call_ms_with_amax_pass": round(ms_call, 4), "call_achieved": round(a_call, 1),
+            "call_frac": round(a_call / hbm, 4),
+            "traffic": _committed_json("quant_dual_traffic.json", "dram_bytes_per_launch"),
+            "traffic_call": _committed_json("quant_dual_traffic.json", "dram_bytes_per_call")}
+
+
+def sweep_point(nv, stream, peaks, args, log2_n=30):
+    """The quantise-only sweep's largest point (2^30 elements: 4096 x 262144
+    bf16, N(0,1) with 0.1% x100 outliers) in its three modes, each with the
+    amax pass and single-pass (amax supplied).  GB/s counts algorithmic bytes
+    (2.5625 B/elem); the input (2 GiB) is larger than L2."""
+    from workloads import sweep_spec
+    spec = sweep_spec(log2_n)
+    R, C = spec.rows, spec.cols
+    x = make_bf16(spec, device=stream.device)
+    o_row = nv.empty_nvfp4(R, C, device=stream.device)
+    o_col = nv.empty_nvfp4(C, R, device=stream.device)
+    ain = x.abs().max().float().reshape(1)
+    torch.cuda.synchronize()
+    nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(3), None, o_col, stream)
+    stream.synchronize()
+    ain_rht = o_col.amax.clone()
+    modes = {
+        "1d_rne": lambda a: nv.nvfp4_quantize(x, nv.BLOCK_1D, 0, a, o_row, stream),
+        "2d": lambda a: nv.nvfp4_quantize(x, nv.BLOCK_2D, 0, a, o_row, stream),
+        "rht_sr_transposed": lambda a: nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(3), a, o_col,
+                                                                stream),
+    }
+    out = {"elements": R * C, "rows": R, "cols": C, "peak_gbs": peaks["hbm_gbs"]}
+    reps = max(5, min(args.steps, 10))
+    for name, fn in modes.items():
+        a_in = ain_rht if name.startswith("rht") else ain
+        for tag, arg in (("with_amax_pass", None), ("amax_supplied", a_in)):
+            ms = _event_ms(lambda: fn(arg), stream, reps)
+            gbs = QUANT_BYTES_PER_ELEM * R * C / (ms * 1e-3) / 1e9
+            out[f"{name}_{tag}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                                    "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    nv.check_status(stream)
+    del x, o_row, o_col
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(nv, step, stream, device, args):
@@ -711,6 +838,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="quantise-only sweep, 2^20 .. 2^30 elements")
     ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS BF16/FP8 context timings")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 2^30-element quantise-only point")
     ap.add_argument("--case", action="append", default=[],
                     help="time single ops instead of the step: gemm:M,N,K or quant:MODE:ROWS,COLS")
     args = ap.parse_args()

@@ -181,9 +181,10 @@ int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, 
 int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc,
                nvfp4_stream_t stream);
 
-/* Synchronise `stream`, then read and clear the device status word of the
- * current device.  Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, NVFP4_ERR_NONFINITE
- * or NVFP4_ERR_CUDA. */
+/* Synchronise `stream`, then read the device status word of the current
+ * device and clear the bits it read (a bit raised meanwhile by a kernel on
+ * another stream stays set for the next call).  Returns NVFP4_OK,
+ * NVFP4_ERR_TIMEOUT, NVFP4_ERR_NONFINITE or NVFP4_ERR_CUDA. */
 int nvfp4_check_status(nvfp4_stream_t stream);
 
 /* Static description of a status code. */
@@ -201,6 +202,23 @@ int nvfp4_version(void);
  * stays usable.  This is how a lost arrival inside a kernel surfaces; no
  * kernel traps or spins without a limit.  Not part of the pages' method. */
 int nvfp4_selftest_wait_timeout(uint32_t limit_us, nvfp4_stream_t stream);
+
+/* ---- FP4 tensor-core rate probe ------------------------------------------- */
+/* Measure the dense FP4 tensor-core rate this library's GEMM is bounded by:
+ * one CTA pair per two multiprocessors issues n_mma (1 .. 2^20) back-to-back
+ * block-scaled pair MMAs (kind::mxf4nvf4, scale_vec::4X, M = 256 over the
+ * pair, N = mma_n (128 or 256), K = 64) on fixed on-chip operands, with no
+ * memory traffic.  For pair p, out[2 p] receives the SM cycles and
+ * out[2 p + 1] the nanoseconds from the first issue to the completion of the
+ * last MMA (0 if a bounded wait expired).  out is device memory with room for
+ * 2 * (multiprocessors / 2) uint64 values (8-byte aligned); *pairs_launched
+ * (host) receives the number of pairs.  FLOP per SM per MMA = 2 * 128 *
+ * mma_n * 64.  The fifth-generation tensor cores' NVFP4 block scaling in
+ * hardware is the pages' basis for this path ("NVFP4: cos'è e come supera
+ * FP8 e BF16 ...", section "Blackwell Architecture: la potenza dietro NVFP4");
+ * the probe is the measured denominator of the GEMM's roofline. */
+int nvfp4_mma_rate_probe(int32_t n_mma, int32_t mma_n, uint64_t* out, int32_t* pairs_launched,
+                         nvfp4_stream_t stream);
 
 /* ---- codec diagnostics (exhaustive conversion checks) -------------------- */
 /* out[i] = E2M1 code (low nibble) of v[i] with round-to-nearest-even,

@@ -46,6 +46,7 @@ EXPORTED = (
     "nvfp4_gemm",
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3", "nvfp4_selftest_wait_timeout",
+    "nvfp4_mma_rate_probe",
 )
 
 
@@ -100,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_version.argtypes = []
     L.nvfp4_selftest_wait_timeout.restype = ctypes.c_int
     L.nvfp4_selftest_wait_timeout.argtypes = [u32, vp]
+    L.nvfp4_mma_rate_probe.restype = ctypes.c_int
+    L.nvfp4_mma_rate_probe.argtypes = [ctypes.c_int32, ctypes.c_int32, vp, ctypes.POINTER(ctypes.c_int32), vp]
     L.nvfp4_encode_e2m1_rne.restype = ctypes.c_int
     L.nvfp4_encode_e2m1_rne.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e2m1_sr.restype = ctypes.c_int
@@ -235,6 +238,43 @@ def nvfp4_check_status(stream=None) -> int:
 
 def nvfp4_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     _check(load_library().nvfp4_selftest_wait_timeout(limit_us, _stream(stream)), "nvfp4_selftest_wait_timeout")
+
+
+def nvfp4_mma_rate_probe(n_mma: int, mma_n: int, out: torch.Tensor, stream=None) -> int:
+    """Run the FP4 MMA-rate probe; out (int64, device) receives cycles and
+    nanoseconds per CTA pair.  Returns the number of pairs launched."""
+    _require_cuda(out)
+    if out.dtype != torch.int64:
+        raise Nvfp4Error("out must be int64")
+    pairs = ctypes.c_int32(0)
+    _check(load_library().nvfp4_mma_rate_probe(n_mma, mma_n, out.data_ptr(), ctypes.byref(pairs), _stream(stream)),
+           "nvfp4_mma_rate_probe")
+    return int(pairs.value)
+
+
+def measure_mma_rate(n_mma: int = 8192, mma_n: int = 256, device=None) -> dict:
+    """Dense FP4 tensor-core rate from the probe: cycles per pair MMA (median
+    over the pairs), FLOP per SM per cycle, the SM clock seen by the probe
+    (cycles / nanoseconds) and the implied whole-GPU TFLOP/s at that clock."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.zeros(2 * (sms // 2), dtype=torch.int64, device=dev)
+    pairs = nvfp4_mma_rate_probe(n_mma, mma_n, out)
+    torch.cuda.synchronize(dev)
+    check_status()
+    v = out.view(-1, 2)[:pairs].cpu()
+    cyc = sorted(int(c) for c in v[:, 0])
+    ns = sorted(int(t) for t in v[:, 1])
+    if cyc[0] == 0:
+        raise Nvfp4Error("MMA-rate probe: a bounded wait expired")
+    c_med, t_med = cyc[len(cyc) // 2], ns[len(ns) // 2]
+    flop_per_sm = 2.0 * 128 * mma_n * 64
+    per_mma = c_med / n_mma
+    ghz = c_med / t_med
+    return {"n_mma": n_mma, "mma": f"M=256 (pair) N={mma_n} K=64 kind::mxf4nvf4 scale_vec::4X", "pairs": pairs,
+            "cycles_per_mma": round(per_mma, 2), "flop_per_sm_per_cycle": round(flop_per_sm / per_mma, 1),
+            "probe_sm_ghz": round(ghz, 4), "sms": sms,
+            "tflops_at_probe_clock": round(flop_per_sm / per_mma * sms * ghz * 1e9 / 1e12, 1)}
 
 
 def nvfp4_encode_e2m1_rne(v: torch.Tensor, out: torch.Tensor, stream=None) -> None:

@@ -10,6 +10,10 @@ namespace nvfp4 {
 // One status word per device (bits kStatusTimeout / kStatusNonFinite).
 __device__ uint32_t g_status_word;
 
+// Clears exactly the bits the host has read, so a bit that a kernel on
+// another stream raises between the read and the clear survives.
+__global__ void status_clear_kernel(uint32_t* status, uint32_t bits) { atomicAnd(status, ~bits); }
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -88,7 +92,9 @@ int quantize_common(const void* x, int64_t rows, int64_t cols, int64_t ld, uint3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (rows == 0 || cols == 0) {
     // empty tensor: amax = s_g = 0 (or the supplied amax), nothing else to write
-    if (amax_in) {
+    if (amax_in == out->amax) {
+      // supplied in place: already holds the amax
+    } else if (amax_in) {
       if (cudaMemcpyAsync(out->amax, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     } else if (cudaMemsetAsync(out->amax, 0, sizeof(float), s) != cudaSuccess) {
@@ -159,7 +165,9 @@ int nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ld, u
     for (int k = 0; k < 2; ++k) {
       const nvfp4_tensor* o = k ? out_col : out_row;
       const float* ain = k ? amax_col_in : amax_row_in;
-      if (ain) {
+      if (ain == o->amax) {
+        // supplied in place: already holds the amax
+      } else if (ain) {
         if (cudaMemcpyAsync(o->amax, ain, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess) return NVFP4_ERR_CUDA;
       } else if (cudaMemsetAsync(o->amax, 0, sizeof(float), s) != cudaSuccess) {
         return NVFP4_ERR_CUDA;
@@ -223,10 +231,12 @@ int nvfp4_check_status(nvfp4_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
   uint32_t word = 0;
-  if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   if (word) {
-    const uint32_t zero = 0;
-    if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return NVFP4_ERR_CUDA;
+    nvfp4::status_clear_kernel<<<1, 1, 0, s>>>(d->status, word);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
   if (word & nvfp4::kStatusTimeout) return NVFP4_ERR_TIMEOUT;
   if (word & nvfp4::kStatusNonFinite) return NVFP4_ERR_NONFINITE;
@@ -253,6 +263,21 @@ int nvfp4_selftest_wait_timeout(uint32_t limit_us, nvfp4_stream_t stream) {
   int rc = check_device(&dev);
   if (rc) return rc;
   return nvfp4::selftest_wait_launch(*dev, (uint64_t)limit_us * 1000ull, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_mma_rate_probe(int32_t n_mma, int32_t mma_n, uint64_t* out, int32_t* pairs_launched,
+                         nvfp4_stream_t stream) {
+  if (n_mma < 1 || n_mma > (1 << 20) || (mma_n != 128 && mma_n != 256) || !out || !pairs_launched)
+    return NVFP4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return NVFP4_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  int rc = check_device(&dev);
+  if (rc) return rc;
+  int pairs = 0;
+  rc = nvfp4::mma_rate_launch(*dev, n_mma, mma_n, reinterpret_cast<unsigned long long*>(out), &pairs,
+                              reinterpret_cast<cudaStream_t>(stream));
+  if (rc == NVFP4_OK) *pairs_launched = pairs;
+  return rc;
 }
 
 int nvfp4_encode_e2m1_rne(const float* v, int64_t n, uint8_t* out, nvfp4_stream_t stream) {

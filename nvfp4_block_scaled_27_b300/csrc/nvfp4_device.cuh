@@ -34,16 +34,19 @@ __device__ __forceinline__ float e4m3_decode(uint32_t code) {
 }
 
 // ------------------------------------------------------------------ E2M1 --
-// Two magnitudes (>= 0) -> one byte of E2M1 codes, round-to-nearest-even with
-// saturation at 6; a0 lands in the low nibble.  Feeding magnitudes keeps the
-// sign decision out of the conversion; the caller ORs the sign bits in.
-__device__ __forceinline__ uint32_t e2m1x2_rne_mag(float a0, float a1) {
-  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a0, a1), __NV_E2M1, cudaRoundNearest);
+// Two values -> one byte of E2M1 codes, round-to-nearest-even, saturating at
+// +-6, sign kept (a negative value that rounds to zero keeps its sign bit:
+// code 0x8); s0 lands in the low nibble.  The hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_rne(float s0, float s1) {
+  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(s0, s1), __NV_E2M1, cudaRoundNearest);
 }
 
-// Stochastic rounding of a magnitude a >= 0: the E2M1 code (0..7) given
-// u64 = u << 6 for 16 random bits u.  With lo <= a < hi adjacent E2M1
-// magnitudes the value rounds up iff u * 2^-16 < (a - lo) / (hi - lo).
+// Stochastic rounding of two values s0, s1 (already scaled by their block's
+// encoding factor) with one 32-bit random word r: s0 takes the low half-word
+// u0, s1 the high half-word u1.  With lo <= a = |s| < hi adjacent E2M1
+// magnitudes, a rounds up iff u * 2^-16 < (a - lo) / (hi - lo); a >= 6
+// saturates to 6; the sign is kept.  Returns a word whose top byte is
+// code0 | code1 << 4 (the other bytes are scratch).
 //
 // Scaled by 2^-126, every E2M1 magnitude below 8 lands on a multiple of 2^22
 // in the fp32 bit pattern b (0.5 -> 1 << 22, 1 -> 2 << 22, 1.5 -> 3 << 22,
@@ -51,17 +54,37 @@ __device__ __forceinline__ uint32_t e2m1x2_rne_mag(float a0, float a1) {
 // values are subnormal or in the first normal binade (uniform spacing
 // 2^-149, i.e. b = a * 2^23), above 2 the top mantissa bit is the E2M1 one.
 // So lo = b >> 22 and (a - lo) / (hi - lo) = (b mod 2^22) / 2^22, and the
-// rule is "round up iff (b mod 2^22) > u * 64", i.e. add 2^22 - 1 - 64 u and
-// keep the bits above 22.  The scaling is exact for a >= 1; below 1 it is
-// rounded UP (ceil(a * 2^23)), which leaves every comparison of a * 2^23
+// rule is "round up iff (b mod 2^22) > 64 u": the magnitude code is
+// (b + 2^22 - 1 - 64 u) >> 22.  The scaling is exact for a >= 1; below 1 it
+// is rounded UP (ceil(a * 2^23)), which leaves every comparison of a * 2^23
 // against an integer threshold unchanged, so the decision equals the exact
-// rule.  Codes above 7 (a >= 6, after rounding) saturate to 7.
-__device__ __forceinline__ uint32_t e2m1_sr_code(float a, uint32_t u64) {
-  const uint32_t b = __float_as_uint(__fmul_ru(a, 0x1p-126f));
-  return min((b + 0x3FFFFFu - u64) >> 22, 7u);
+// rule.  Clamping a to 6 first keeps the code at most 7 (b <= 7 << 22, and 6
+// itself never rounds up).
+//
+// The code of s0 is formed directly in bits 24..27 of
+//   x0 = 4 b0 + (2^24 - 1 - 256 u0) + sign0 * 2^27
+// (four times the sum above plus 3, which does not change the quotient by
+// 2^24; x0 < 2^28), and the code of s1 in bits 28..31 of
+//   x1 = 64 b1 + (2^28 - 1 - 4096 u1) + sign1 * 2^31,
+// so the pair's byte is the top byte of x0 | (x1 & 0xF0000000).  256 u0 and
+// 256 u1 are byte permutations of r.
+__device__ __forceinline__ uint32_t sr_pair_b3(float s0, float s1, uint32_t r) {
+  const float a0 = fminf(fabsf(s0), 6.0f), a1 = fminf(fabsf(s1), 6.0f);
+  const uint32_t b0 = __float_as_uint(__fmul_ru(a0, 0x1p-126f));
+  const uint32_t b1 = __float_as_uint(__fmul_ru(a1, 0x1p-126f));
+  const uint32_t m0 = __byte_perm(r, 0u, 0x4104);  // u0 << 8
+  const uint32_t m1 = __byte_perm(r, 0u, 0x4324);  // u1 << 8
+  const uint32_t g0 = ((__float_as_uint(s0) >> 4) & 0x08000000u) | 0x00FFFFFFu;
+  const uint32_t g1 = (__float_as_uint(s1) & 0x80000000u) | 0x0FFFFFFFu;
+  const uint32_t x0 = b0 * 4u + (g0 - m0);
+  const uint32_t x1 = b1 * 64u + (g1 - m1 * 16u);
+  return x0 | (x1 & 0xF0000000u);
 }
 
-__device__ __forceinline__ uint32_t sign_nibble(float v) { return (__float_as_uint(v) >> 31) << 3; }
+// The top bytes of four words, in order, as one word.
+__device__ __forceinline__ uint32_t top_bytes4(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3) {
+  return __byte_perm(__byte_perm(p0, p1, 0x0073), __byte_perm(p2, p3, 0x0073), 0x5410);
+}
 
 // ------------------------------------------------------------------ hash --
 // "lowbias32" 32-bit integer finaliser (C. Wellons, hash-prospector, 2018):
@@ -138,10 +161,11 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 }
 
 // The 16-point transform of two columns at once (lane 0: column a, lane 1:
-// column b), same operation order as rht16: sign flips, butterflies with
-// strides 1, 2, 4, 8, then the exact 1/4.
-__device__ __forceinline__ void rht16x2(float (&a)[16], float (&b)[16], uint32_t signs) {
-  uint64_t v[16];
+// column b) without the final 1/4: sign flips, then butterflies with strides
+// 1, 2, 4, 8, in the definition's operation order.  Every result lies on the
+// 2^-133 grid of its bf16 inputs, so the 1/4 that follows is exact and can be
+// applied wherever it is cheapest (once to an amax, for instance).
+__device__ __forceinline__ void rht16x2_unscaled(float (&a)[16], float (&b)[16], uint32_t signs, uint64_t (&v)[16]) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float d = ((signs >> j) & 1u) ? -1.0f : 1.0f;
@@ -158,6 +182,19 @@ __device__ __forceinline__ void rht16x2(float (&a)[16], float (&b)[16], uint32_t
       }
     }
   }
+}
+
+__device__ __forceinline__ void rht16x2_unscaled(float (&a)[16], float (&b)[16], uint32_t signs) {
+  uint64_t v[16];
+  rht16x2_unscaled(a, b, signs, v);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) f2_unpack(v[j], a[j], b[j]);
+}
+
+// The full transform of two columns: the butterflies, then the exact 1/4.
+__device__ __forceinline__ void rht16x2(float (&a)[16], float (&b)[16], uint32_t signs) {
+  uint64_t v[16];
+  rht16x2_unscaled(a, b, signs, v);
   const uint64_t q = f2_pack(0.25f, 0.25f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) f2_unpack(f2_mul(v[j], q), a[j], b[j]);
@@ -177,20 +214,11 @@ __device__ __forceinline__ float block_enc(float sg, uint32_t sc) {
   return (scf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sg, scf));
 }
 
-// Encode 16 values with a common factor into 8 bytes (two 32-bit words),
-// round-to-nearest-even.
-__device__ __forceinline__ uint2 encode16_rne(const float (&v)[16], float enc) {
-  const uint64_t e2 = f2_pack(enc, enc);
-  uint32_t w[2] = {0u, 0u};
-#pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    float s0, s1;
-    f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), e2), s0, s1);
-    uint32_t byte = e2m1x2_rne_mag(fabsf(s0), fabsf(s1));
-    byte |= sign_nibble(s0) | (sign_nibble(s1) << 4);
-    w[j / 8] |= byte << (8 * ((j / 2) % 4));
-  }
-  return make_uint2(w[0], w[1]);
+// Every encoding factor of a tensor (one per E4M3 code; codes above 0x7E
+// never occur) into shared memory, by the whole CTA.  The caller
+// synchronises before use.
+__device__ __forceinline__ void fill_enc_table(float* tab, float sg) {
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) tab[c] = block_enc(sg, (uint32_t)c);
 }
 
 // Random words of the 8 pairs q0 .. q0 + 7 of a 16-element block (q0 a
@@ -205,55 +233,42 @@ __device__ __forceinline__ void sr_words8(uint32_t hk, uint32_t q0lo, uint32_t (
   for (int j = 0; j < 8; ++j) w[j] = mix32_tail(g ^ (uint32_t)j);
 }
 
-// SR codes (sign included) of two values s0, s1 (already scaled by the
-// block's encoding factor) from one random word r: s0 uses the low
-// half-word, s1 the high half-word.  Returns c0 | c1 << 4.  (Moving the
-// threshold and packing arithmetic onto high products and multiply-adds
-// measured slower.)
-__device__ __forceinline__ uint32_t sr_pair_codes(float s0, float s1, uint32_t r) {
-  const uint32_t c0 = e2m1_sr_code(fabsf(s0), (r << 6) & 0x3FFFC0u) | sign_nibble(s0);
-  const uint32_t c1 = e2m1_sr_code(fabsf(s1), (r >> 10) & 0x3FFFC0u) | sign_nibble(s1);
-  return c0 | (c1 << 4);
-}
-
-// SR codes of 16 values already multiplied by the block's encoding factor.
+// SR codes of 16 values already multiplied by the block's encoding factor:
+// hk is the hash key of the block's pair range, q0 the pair index of element
+// 0 (8 pairs, one hash word each; the even element uses the low half-word).
 __device__ __forceinline__ uint2 encode16_sr_scaled(const float (&sv)[16], uint32_t hk, uint64_t q0) {
   uint32_t r[8];
   sr_words8(hk, (uint32_t)q0, r);
-  uint32_t w[2] = {0u, 0u};
+  uint32_t p[8];
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) w[j / 8] += sr_pair_codes(sv[j], sv[j + 1], r[j / 2]) << (8 * ((j / 2) % 4));
-  return make_uint2(w[0], w[1]);
+  for (int j = 0; j < 8; ++j) p[j] = sr_pair_b3(sv[2 * j], sv[2 * j + 1], r[j]);
+  return make_uint2(top_bytes4(p[0], p[1], p[2], p[3]), top_bytes4(p[4], p[5], p[6], p[7]));
 }
 
 // RNE codes of 16 values already multiplied by the block's encoding factor.
 __device__ __forceinline__ uint2 encode16_rne_scaled(const float (&sv)[16]) {
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    uint32_t byte = e2m1x2_rne_mag(fabsf(sv[j]), fabsf(sv[j + 1]));
-    byte |= sign_nibble(sv[j]) | (sign_nibble(sv[j + 1]) << 4);
-    w[j / 8] |= byte << (8 * ((j / 2) % 4));
-  }
+  for (int j = 0; j < 16; j += 2) w[j / 8] |= e2m1x2_rne(sv[j], sv[j + 1]) << (8 * ((j / 2) % 4));
   return make_uint2(w[0], w[1]);
 }
 
-// Same with stochastic rounding: hk is the per-block hash key, q0 the pair
-// index of element 0 (8 pairs, one hash word each; the even element uses the
-// low half-word).
-__device__ __forceinline__ uint2 encode16_sr(const float (&v)[16], float enc, uint32_t hk,
-                                             uint64_t q0) {
-  uint32_t r[8];
-  sr_words8(hk, (uint32_t)q0, r);
+// Scale 16 values by a common factor (packed pairs; each lane one IEEE
+// round-to-nearest multiply).
+__device__ __forceinline__ void scale16(float (&v)[16], float enc) {
   const uint64_t e2 = f2_pack(enc, enc);
-  uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    float s0, s1;
-    f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), e2), s0, s1);
-    w[j / 8] += sr_pair_codes(s0, s1, r[j / 2]) << (8 * ((j / 2) % 4));
-  }
-  return make_uint2(w[0], w[1]);
+  for (int j = 0; j < 16; j += 2) f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), e2), v[j], v[j + 1]);
+}
+
+__device__ __forceinline__ uint2 encode16_rne(float (&v)[16], float enc) {
+  scale16(v, enc);
+  return encode16_rne_scaled(v);
+}
+
+__device__ __forceinline__ uint2 encode16_sr(float (&v)[16], float enc, uint32_t hk, uint64_t q0) {
+  scale16(v, enc);
+  return encode16_sr_scaled(v, hk, q0);
 }
 
 // Offset of scale (row r, block kb) in the MMA layout (cols/64 atoms per

@@ -201,12 +201,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   const int num_kb = p.K / BK;
   const int64_t atoms_per_band = p.K / 64;
 
+  int prod_stage = 0;      // operand producer's ring position (thread 0)
+  uint32_t prod_phase = 0;
   if (warp == 0) {
     // ------------------------------------------------- operand producer --
     if (lane == 0) {
       const uint32_t leader_full = mapa_shared(bar_full, 0);
-      int stage = 0;
-      uint32_t phase = 0;
+      int& stage = prod_stage;
+      uint32_t& phase = prod_phase;
       for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
         int tm, tn;
         tile_coords(p, t, tm, tn);
@@ -440,9 +442,21 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   __syncthreads();
   if (threadIdx.x == 0) {
     mbar_wait_cluster(bar_mma_done, 0, p.status, 10000000000ull);
-    // After an abort this CTA's operand copies (which complete on the
-    // leader's barrier, not on one it can watch) may still be in flight:
-    // give them time to land in its shared memory before it can exit.
+    // Both CTAs' operand copies complete on the leader's `full` barriers.
+    // The leader waits (bounded) for the last phase it armed on every stage,
+    // so neither CTA releases its shared memory while a copy it armed can
+    // still land; in a run without an abort every such phase has completed
+    // (the MMA warp consumed it) and these waits return at once.  A stage
+    // never armed passes at once too (parity of the phase before the first).
+    if (rank == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t par = (s < prod_stage) ? prod_phase : (prod_phase ^ 1u);
+        mbar_wait(bar_full + 8 * s, par, p.status, 100000000ull);
+      }
+    }
+    // After an abort the peer may also have issued copies for a stage the
+    // leader never armed, which no barrier here can observe: give those time
+    // to land before either CTA can exit.
     if (*abort_flag) {
       const uint64_t t0 = globaltimer_ns();
       while (globaltimer_ns() - t0 < 200000ull) {}
@@ -452,6 +466,71 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   }
   __syncthreads();
   if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------- MMA-rate probe --
+// Measures the issue-to-completion time of a run of back-to-back pair MMAs of
+// the GEMM's kind (kind::mxf4nvf4 block_scale scale_vec::4X, M = 256 over the
+// pair, the given N, K = 64) with no data movement: thread 0 of the leader
+// CTA issues n_mma MMAs on fixed shared-memory operands and fixed scale
+// columns (their contents do not matter for the timing), commits them to an
+// mbarrier in both CTAs and waits for it.  out[2 p] = SM cycles (clock64)
+// and out[2 p + 1] = nanoseconds (globaltimer) of pair p, from before the
+// first issue to the commit's arrival.  Every wait is bounded.
+constexpr int PROBE_THREADS = 128;
+constexpr int PROBE_OFF_BAR = A_BYTES + B_BYTES;  // operands at 0 and A_BYTES
+constexpr int PROBE_SMEM = PROBE_OFF_BAR + 16 + 1024;
+
+__global__ void __launch_bounds__(PROBE_THREADS, 1)
+mma_rate_kernel(int n_mma, uint32_t idesc, unsigned long long* out, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar = sbase + PROBE_OFF_BAR;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + PROBE_OFF_BAR + 8);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair(sbase + PROBE_OFF_BAR + 8, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) {
+    if (rank == 0) {
+      const unsigned long long c0 = clock64();
+      const uint64_t t0 = globaltimer_ns();
+      const uint64_t ad = smem_desc(sbase, 16, 1024, 2);
+      const uint64_t bd = smem_desc(sbase + A_BYTES, 16, 1024, 2);
+      for (int i = 0; i < n_mma; ++i) {
+        const uint32_t j = (uint32_t)(i & 3);
+        tc_mma_nvf4_pair(tmem_base, ad + 2 * j, bd + 2 * j, idesc, tmem_base + 256u + 4u * j,
+                         tmem_base + 256u + 16u + 8u * j, i > 0 ? 1u : 0u);
+      }
+      tc_commit_pair(bar, 0x3);
+      const bool ok = mbar_wait_cluster(bar, 0, status);
+      const unsigned long long c1 = clock64();
+      const uint64_t t1 = globaltimer_ns();
+      const int pair = (int)cluster_id_x();
+      out[2 * pair] = ok ? c1 - c0 : 0ull;
+      out[2 * pair + 1] = ok ? t1 - t0 : 0ull;
+    } else {
+      (void)mbar_wait_cluster(bar, 0, status);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
@@ -572,6 +651,59 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, ta, tb, tc, p) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4
+
+namespace nvfp4 {
+
+int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long long* out, int* pairs_out,
+                    cudaStream_t stream) {
+  using namespace gemm;
+  static std::mutex mu;
+  static int max_pairs[64] = {};
+  int pairs = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) return NVFP4_ERR_CUDA;
+    if (max_pairs[dev.device] == 0) {
+      if (cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROBE_SMEM) !=
+          cudaSuccess)
+        return NVFP4_ERR_CUDA;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+      cfg.blockDim = dim3(PROBE_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = PROBE_SMEM;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, mma_rate_kernel, &cfg) != cudaSuccess || n <= 0) return NVFP4_ERR_CUDA;
+      // one pair per two SMs (a pair per SM pair, as the GEMM runs)
+      max_pairs[dev.device] = n < dev.sm_count / 2 ? n : dev.sm_count / 2;
+    }
+    pairs = max_pairs[dev.device];
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(PROBE_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PROBE_SMEM;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mma_rate_kernel, n_mma, make_idesc(BM_PAIR, mma_n), out, dev.status) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  *pairs_out = pairs;
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

@@ -40,6 +40,10 @@ int quantize_mx_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
                 int64_t ldc, cudaStream_t stream);
 
+// FP4 MMA-rate probe (arguments validated by the caller).
+int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long long* out, int* pairs_out,
+                    cudaStream_t stream);
+
 // Bounded-wait self-test.
 int selftest_wait_launch(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
 

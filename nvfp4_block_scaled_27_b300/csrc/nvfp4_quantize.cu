@@ -8,17 +8,23 @@
 // readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph.
 //
 // Kernels
-//   amax_*        : one read of the input, per-thread max, warp-shuffle and
-//                   CTA reduction, one atomicMax per CTA into the fp32 amax.
-//   quant_rows_*  : row-wise blocks straight from registers; a warp reads
-//                   1 KiB of contiguous input per 16-element step (1D) and
-//                   writes 256 contiguous code bytes.
+//   amax_plain    : one read of the input, eight 16-byte loads in flight per
+//                   thread, packed bf16 integer max, one atomicMax per CTA.
+//   amax_tile     : 64 x 256 input tiles staged in shared memory; the plain
+//                   amax and/or the amax after the column-wise transform.
+//   amax_rht_rows : amax after the row-wise transform.
+//   quant_rows_*  : row-wise blocks straight from registers (1D) or from a
+//                   staged tile (2D); a warp reads 1 KiB of contiguous input
+//                   per 16-element step and writes 256 contiguous code bytes.
 //   quant_cols    : blocks along the input's rows (transposed output): a
 //                   64 x 256 input tile is staged in shared memory with
-//                   coalesced 16-byte loads, then each thread owns a column
+//                   coalesced 16-byte copies, then each thread owns a column
 //                   pair and walks four 16-row chunks.
-// All arithmetic on values is single-rounded IEEE fp32 (no contraction), so
-// results are bit-reproducible.
+//   quant_dual    : both operands of one tensor from one staged tile.
+// Every CTA keeps the tensor's 128 encoding factors 1 / (s_g * scale) in
+// shared memory, so a block's factor is one lookup.  All arithmetic on
+// values is single-rounded IEEE fp32 (no contraction), so results are
+// bit-reproducible.
 #include <float.h>
 
 #include <mutex>
@@ -39,7 +45,7 @@ struct QuantParams {
   float* amax_out;        // written once when amax came from the caller, else null
   float* sg_out;
   uint32_t* status;
-  uint32_t sr_key;
+  uint32_t sr_hk[2];      // hash key of pair indices with hi32 = 0 and 1: mix32(key ^ hi32)
   uint32_t rht_signs;
 };
 
@@ -65,6 +71,21 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
+}
+
+// max(|a|, |b|, |c|) in one instruction (three-input max over magnitudes).
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float r;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max |v[j]| over 16 values.
+__device__ __forceinline__ float absmax16(const float (&v)[16]) {
+  float m = absmax3(v[0], v[1], v[2]);
+#pragma unroll
+  for (int j = 3; j < 15; j += 2) m = absmax3(m, v[j], v[j + 1]);
+  return absmax3(m, v[15], v[15]);
 }
 
 // CTA-wide max of a non-negative fp32 bit pattern, then one atomicMax.
@@ -106,6 +127,12 @@ __device__ __forceinline__ float tensor_scale(const QuantParams& p, float& amax)
   return sg;
 }
 
+// Hash key of the pair range starting at pair index q0 (the tensor has fewer
+// than 2^34 elements, so hi32(q0) is 0 or 1).
+__device__ __forceinline__ uint32_t pair_key(const QuantParams& p, uint64_t q0) {
+  return (q0 >> 32) ? p.sr_hk[1] : p.sr_hk[0];
+}
+
 // ----------------------------------------------------------------- amax --
 // Plain amax of a bf16 matrix (vpr 16-byte vectors per row, row stride ldv
 // vectors).  Magnitudes are compared as integers (exact for bf16).  Eight
@@ -134,10 +161,11 @@ __global__ void __launch_bounds__(256) amax_plain_kernel(const uint4* __restrict
 }
 
 // amax after the row-wise transform: every 16 consecutive elements of a row.
+// max |1/4 w| = 1/4 max |w| exactly, so the 1/4 is applied once at the end.
 __global__ void __launch_bounds__(256) amax_rht_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                             int64_t cols, int64_t ld, uint32_t signs,
                                                             float* out) {
-  uint32_t m = 0u;
+  float m = 0.0f;
   const uint32_t nb = (uint32_t)(cols / 16);
   const uint32_t total = (uint32_t)(rows * nb);
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -146,44 +174,13 @@ __global__ void __launch_bounds__(256) amax_rht_rows_kernel(const uint16_t* __re
     float v[16];
     unpack16(ldg_nc(src), ldg_nc(src + 1), v);
     rht16(v, signs);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(fabsf(v[j])));
+    m = fmaxf(m, absmax16(v));
   }
-  cta_amax_commit(m, out);
-}
-
-// amax after the column-wise transform: every 16 consecutive rows of a
-// column.  A thread owns 16 rows x 8 columns (one 16-byte vector per row).
-__global__ void __launch_bounds__(256) amax_rht_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                            int64_t cols, int64_t ld, uint32_t signs,
-                                                            float* out) {
-  uint32_t m = 0u;
-  const uint32_t nv = (uint32_t)(cols / 8);
-  const uint32_t total = (uint32_t)((rows / 16) * nv);
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const uint32_t rc = i / nv, vc = i - rc * nv;
-    const uint16_t* base = x + (int64_t)rc * 16 * ld + (int64_t)vc * 8;
-    uint4 u[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) u[k] = ldg_nc(base + (int64_t)k * ld);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float v[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t w = (c < 2) ? u[k].x : (c < 4) ? u[k].y : (c < 6) ? u[k].z : u[k].w;
-        v[k] = (c & 1) ? bf16_hi(w) : bf16_lo(w);
-      }
-      rht16(v, signs);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) m = max(m, __float_as_uint(fabsf(v[k])));
-    }
-  }
-  cta_amax_commit(m, out);
+  cta_amax_commit(__float_as_uint(m), out);
 }
 
 // Two CTA-wide maxima at once (one shared scratch, one barrier), then one
-// atomicMax each.
+// atomicMax each (a null output is skipped).
 __device__ __forceinline__ void cta_amax_commit2(uint32_t m1, float* out1, uint32_t m2, float* out2) {
   __shared__ uint32_t red2[2][32];
   m1 = warp_max_u32(m1);
@@ -199,62 +196,106 @@ __device__ __forceinline__ void cta_amax_commit2(uint32_t m1, float* out1, uint3
     m1 = warp_max_u32(in ? red2[0][lane] : 0u);
     m2 = warp_max_u32(in ? red2[1][lane] : 0u);
     if (lane == 0) {
-      if (m1 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out1), m1);
-      if (m2 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out2), m2);
+      if (out1 && m1 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out1), m1);
+      if (out2 && m2 != 0u) atomicMax(reinterpret_cast<unsigned int*>(out2), m2);
     }
   }
 }
 
-// Both amaxes the dual-orientation quantiser needs, from one read: the plain
-// amax (row-wise operand) and the amax after the column-wise transform
-// (transposed operand).  A thread owns 16 rows x 8 columns.
-__global__ void __launch_bounds__(256) amax_dual_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                                        int64_t ld, uint32_t signs, float* out_plain,
-                                                        float* out_rht) {
-  uint32_t mp = 0u, mr = 0u;
-  const uint32_t nv = (uint32_t)(cols / 8);
-  const uint32_t total = (uint32_t)((rows / 16) * nv);
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const uint32_t rc = i / nv, vc = i - rc * nv;
-    const uint16_t* base = x + (int64_t)rc * 16 * ld + (int64_t)vc * 8;
-    uint4 u[16];
+// ------------------------------------------------------ staged tiles --
+constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
+constexpr int kColTileCols = 256;  // input columns per tile
+constexpr int kColThreads = 128;   // one thread per column pair
+
+// Stage the tile (r0, c0) of the input in shared memory with asynchronous
+// 16-byte copies (all of a thread's copies in flight at once, no registers
+// held); a warp moves one 512-byte input row segment per step and elements
+// outside the input are zero-filled.  Ends with the copies complete and the
+// tile visible to the whole CTA.
+__device__ __forceinline__ void stage_tile(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                           uint32_t (&tile)[kColTileRows][kColTileCols / 2], int64_t r0,
+                                           int64_t c0) {
+  const int tid = threadIdx.x;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) u[k] = ldg_nc(base + (int64_t)k * ld);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) mp = absmax_pairs(mp, u[k]);
-#pragma unroll
-    for (int c = 0; c < 8; c += 2) {
-      float v0[16], v1[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t w = (c < 2) ? u[k].x : (c < 4) ? u[k].y : (c < 6) ? u[k].z : u[k].w;
-        v0[k] = bf16_lo(w);
-        v1[k] = bf16_hi(w);
-      }
-      rht16x2(v0, v1, signs);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) mr = max(mr, max(__float_as_uint(fabsf(v0[k])), __float_as_uint(fabsf(v1[k]))));
-    }
+  for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
+    const int idx = k * kColThreads + tid;
+    const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
+    const bool ok = r0 + row < rows && c0 + vec * 8 < cols;
+    const uint16_t* src = ok ? x + (r0 + row) * ld + c0 + vec * 8 : x;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(&tile[row][vec * 4])), "l"(src),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
   }
-  cta_amax_commit2(pairs_to_f32_bits(mp), out_plain, mr, out_rht);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+}
+
+__device__ __forceinline__ void stage_tile(const QuantParams& p, uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                           int64_t r0, int64_t c0) {
+  stage_tile(p.x, p.rows, p.cols, p.ld, tile, r0, c0);
+}
+
+// The 32 values of a thread's column pair in one 16-row chunk of a staged
+// tile (v0: column 2 tid, v1: column 2 tid + 1).
+__device__ __forceinline__ void load_chunk_cols(const uint32_t (&tile)[kColTileRows][kColTileCols / 2], int k,
+                                                float (&v0)[16], float (&v1)[16]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t w = tile[16 * k + i][tid];
+    v0[i] = bf16_lo(w);
+    v1[i] = bf16_hi(w);
+  }
+}
+
+// amax of a bf16 matrix over staged 64 x 256 tiles: the plain amax (kPlain)
+// and/or the amax after the column-wise transform (kCols: every 16
+// consecutive rows of a column, 1/4 applied once at the end).  Zero-filled
+// padding does not change either maximum.
+template <bool kPlain, bool kCols>
+__global__ void __launch_bounds__(kColThreads) amax_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ld, uint32_t signs,
+                                                                float* out_plain, float* out_cols) {
+  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  uint32_t mp = 0u;
+  float mc = 0.0f;
+  const int64_t tiles_c = (cols + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = ((rows + kColTileRows - 1) / kColTileRows) * tiles_c;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    stage_tile(x, rows, cols, ld, tile, tr * kColTileRows, tc * kColTileCols);
+#pragma unroll 1
+    for (int k = 0; k < kColTileRows / 16; ++k) {
+      if (kPlain) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mp = __vmaxu2(mp, tile[16 * k + i][threadIdx.x] & 0x7FFF7FFFu);
+      }
+      if (kCols) {
+        float v0[16], v1[16];
+        load_chunk_cols(tile, k, v0, v1);
+        rht16x2_unscaled(v0, v1, signs);
+        mc = absmax3(mc, absmax16(v0), absmax16(v1));
+      }
+    }
+    __syncthreads();
+  }
+  cta_amax_commit2(pairs_to_f32_bits(mp), kPlain ? out_plain : nullptr, __float_as_uint(__fmul_rn(mc, 0.25f)),
+                   kCols ? out_cols : nullptr);
 }
 
 // ------------------------------------------------------- row-wise, 1D --
 template <bool kSR, bool kRHT, bool kMMA>
-__device__ __forceinline__ void quant_block_1d(const QuantParams& p, uint32_t i, uint32_t nb,
-                                               const uint4& a, const uint4& b4, float sg, float den) {
+__device__ __forceinline__ void quant_block_1d(const QuantParams& p, const float* enc_tab, uint32_t i, uint32_t nb,
+                                               const uint4& a, const uint4& b4, float den) {
   float v[16];
   unpack16(a, b4, v);
   if (kRHT) rht16(v, p.rht_signs);
-  float amax_b = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
-  const uint32_t sc = block_scale_code(amax_b, den);
-  const float enc = block_enc(sg, sc);
+  const uint32_t sc = block_scale_code(absmax16(v), den);
+  const float enc = enc_tab[sc];
   uint2 q;
   if (kSR) {
     const uint64_t q0 = (uint64_t)i * 8u;  // element index 16 i, pair index 8 i
-    q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+    q = encode16_sr(v, enc, pair_key(p, q0), q0);
   } else {
     q = encode16_rne(v, enc);
   }
@@ -269,9 +310,12 @@ __device__ __forceinline__ void quant_block_1d(const QuantParams& p, uint32_t i,
 // its elements have output indices 16 i .. 16 i + 15.
 template <bool kSR, bool kRHT, bool kMMA>
 __global__ void __launch_bounds__(256) quant_rows_1d_kernel(QuantParams p) {
+  __shared__ float enc_tab[128];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
+  fill_enc_table(enc_tab, sg);
+  __syncthreads();
   const uint32_t nb = (uint32_t)(p.ocols / 16);
   const uint32_t total = (uint32_t)(p.orows * nb);
   const uint32_t stride = gridDim.x * blockDim.x;
@@ -282,50 +326,25 @@ __global__ void __launch_bounds__(256) quant_rows_1d_kernel(QuantParams p) {
     const uint4* si = reinterpret_cast<const uint4*>(p.x + (int64_t)ri * p.ld + (int64_t)(i - ri * nb) * 16);
     const uint4* sj = reinterpret_cast<const uint4*>(p.x + (int64_t)rj * p.ld + (int64_t)(j - rj * nb) * 16);
     const uint4 a0 = ldg_nc(si), a1 = ldg_nc(si + 1), b0 = ldg_nc(sj), b1 = ldg_nc(sj + 1);
-    quant_block_1d<kSR, kRHT, kMMA>(p, i, nb, a0, a1, sg, den);
-    quant_block_1d<kSR, kRHT, kMMA>(p, j, nb, b0, b1, sg, den);
+    quant_block_1d<kSR, kRHT, kMMA>(p, enc_tab, i, nb, a0, a1, den);
+    quant_block_1d<kSR, kRHT, kMMA>(p, enc_tab, j, nb, b0, b1, den);
   }
   if (i < total) {
     const uint32_t ri = i / nb;
     const uint4* si = reinterpret_cast<const uint4*>(p.x + (int64_t)ri * p.ld + (int64_t)(i - ri * nb) * 16);
-    quant_block_1d<kSR, kRHT, kMMA>(p, i, nb, ldg_nc(si), ldg_nc(si + 1), sg, den);
+    quant_block_1d<kSR, kRHT, kMMA>(p, enc_tab, i, nb, ldg_nc(si), ldg_nc(si + 1), den);
   }
 }
 
 // ------------------------------------------------- column-wise (x^T) --
-constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
-constexpr int kColTileCols = 256;  // input columns per tile
-constexpr int kColThreads = 128;   // one thread per column pair
-
-// Stage the tile (r0, c0) of the input in shared memory with asynchronous
-// 16-byte copies (all of a thread's copies in flight at once, no registers
-// held); a warp moves one 512-byte input row segment per step and elements
-// outside the input are zero-filled.  Ends with the copies complete and the
-// tile visible to the whole CTA.
-__device__ __forceinline__ void stage_tile(const QuantParams& p, uint32_t (&tile)[kColTileRows][kColTileCols / 2],
-                                           int64_t r0, int64_t c0) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
-    const int idx = k * kColThreads + tid;
-    const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
-    const bool ok = r0 + row < p.rows && c0 + vec * 8 < p.cols;
-    const uint16_t* src = ok ? p.x + (r0 + row) * p.ld + c0 + vec * 8 : p.x;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(&tile[row][vec * 4])), "l"(src),
-                 "r"(ok ? 16 : 0)
-                 : "memory");
-  }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-}
-
 // Column-wise (transposed) quantisation of a staged tile.  Output row c =
 // input column c, output column r = input row r.  Blocks run along the
 // input's rows; with kTwoD the 16x16 tile amax is shared by the 8 threads
 // (16 columns) of a tile via shuffles.
 template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
-__device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
-                                          int64_t r0, int64_t c0, float sg, float den) {
+__device__ __forceinline__ void cols_tile(const QuantParams& p, const float* enc_tab,
+                                          const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                          int64_t r0, int64_t c0, float den) {
   const int64_t R = p.rows, C = p.cols;
   const int tid = threadIdx.x;
   const int64_t kb_per_row = R / 16;  // output blocks per output row
@@ -342,24 +361,18 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
   uint2 qa0 = make_uint2(0u, 0u), qa1 = qa0, qa2 = qa0, qa3 = qa0;
   uint2 qb0 = qa0, qb1 = qa0, qb2 = qa0, qb3 = qa0;
   uint32_t sca = 0u, scb = 0u;
+  // pair indices of the two output rows' first elements in this tile; each
+  // 16-row chunk advances them by 8
+  uint64_t pa = ((uint64_t)c * (uint64_t)R + (uint64_t)r0) >> 1;
+  uint64_t pb = pa + (uint64_t)(R >> 1);
 #pragma unroll 1
-  for (int k = 0; k < kColTileRows / 16; ++k) {
+  for (int k = 0; k < kColTileRows / 16; ++k, pa += 8u, pb += 8u) {
     const int64_t rb = r0 + 16 * k;  // first input row of the block
     if (rb >= R) break;              // uniform across the CTA
     float v0[16], v1[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t w = tile[16 * k + i][tid];
-      v0[i] = bf16_lo(w);
-      v1[i] = bf16_hi(w);
-    }
+    load_chunk_cols(tile, k, v0, v1);
     if (kRHT) rht16x2(v0, v1, p.rht_signs);
-    float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      a0 = fmaxf(a0, fabsf(v0[i]));
-      a1 = fmaxf(a1, fabsf(v1[i]));
-    }
+    float a0 = absmax16(v0), a1 = absmax16(v1);
     if (kTwoD) {
       float a = fmaxf(a0, a1);
       a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
@@ -369,15 +382,13 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
     }
     if (!col_ok) continue;
     const uint32_t sc0 = block_scale_code(a0, den), sc1 = block_scale_code(a1, den);
-    const uint64_t e01 = f2_pack(block_enc(sg, sc0), block_enc(sg, sc1));
+    const uint64_t e01 = f2_pack(enc_tab[sc0], enc_tab[sc1]);
 #pragma unroll
     for (int i = 0; i < 16; ++i) f2_unpack(f2_mul(f2_pack(v0[i], v1[i]), e01), v0[i], v1[i]);
     uint2 q0, q1;
     if (kSR) {
-      const uint64_t p0 = ((uint64_t)c * (uint64_t)R + (uint64_t)rb) >> 1;
-      const uint64_t p1 = ((uint64_t)(c + 1) * (uint64_t)R + (uint64_t)rb) >> 1;
-      q0 = encode16_sr_scaled(v0, mix32(p.sr_key ^ (uint32_t)(p0 >> 32)), p0);
-      q1 = encode16_sr_scaled(v1, mix32(p.sr_key ^ (uint32_t)(p1 >> 32)), p1);
+      q0 = encode16_sr_scaled(v0, pair_key(p, pa), pa);
+      q1 = encode16_sr_scaled(v1, pair_key(p, pb), pb);
     } else {
       q0 = encode16_rne_scaled(v0);
       q1 = encode16_rne_scaled(v1);
@@ -423,56 +434,80 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const uint32_t (
 }
 
 template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
-__global__ void __launch_bounds__(kColThreads) quant_cols_kernel(QuantParams p) {
+__global__ void __launch_bounds__(kColThreads, 6) quant_cols_kernel(QuantParams p) {
   __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  __shared__ float enc_tab[128];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
+  fill_enc_table(enc_tab, sg);
   const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
   const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);
-    cols_tile<kSR, kRHT, kTwoD, kMMA>(p, tile, tr * kColTileRows, tc * kColTileCols, sg, den);
+    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);  // its barrier also publishes enc_tab
+    cols_tile<kSR, kRHT, kTwoD, kMMA>(p, enc_tab, tile, tr * kColTileRows, tc * kColTileCols, den);
     __syncthreads();
   }
 }
 
-// Row-wise 1D quantisation of a staged tile: thread t owns 16-column block
-// t % 16 of rows t / 16 + 8 i (i = 0..7); 16 threads write 128 contiguous
-// code bytes of a row.
+// Row-wise 1D quantisation of a staged tile: thread t owns the two
+// 16-column blocks 2 (t % 8) and 2 (t % 8) + 1 of rows t / 8 + 16 i
+// (i = 0..3); 8 threads write 128 contiguous code bytes of a row.  Row and
+// pair indices advance by 16 rows per step, so a step costs no divisions.
+template <bool kSR>
+__device__ __forceinline__ uint2 rows_block(const QuantParams& p, const float* enc_tab, const uint4& a,
+                                            const uint4& b, float den, uint64_t q0, uint32_t& sc) {
+  float v[16];
+  unpack16(a, b, v);
+  sc = block_scale_code(absmax16(v), den);
+  const float enc = enc_tab[sc];
+  return kSR ? encode16_sr(v, enc, pair_key(p, q0), q0) : encode16_rne(v, enc);
+}
+
 template <bool kSR, bool kMMA>
-__device__ __forceinline__ void rows_tile(const QuantParams& p, const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
-                                          int64_t r0, int64_t c0, float sg, float den) {
+__device__ __forceinline__ void rows_tile(const QuantParams& p, const float* enc_tab,
+                                          const uint32_t (&tile)[kColTileRows][kColTileCols / 2],
+                                          int64_t r0, int64_t c0, float den) {
   const int tid = threadIdx.x;
-  const int blk = tid & 15;
-  const int64_t col = c0 + 16 * blk;
-  if (col >= p.cols) return;  // cols % 16 == 0: a block is wholly in or out
-  const int64_t nb = p.cols / 16;
-#pragma unroll 2
-  for (int i = 0; i < kColTileRows / 8; ++i) {
-    const int rl = (tid >> 4) + 8 * i;
-    const int64_t r = r0 + rl;
+  const int bp = tid & 7;                 // block pair within the tile row
+  const int64_t col = c0 + 32 * bp;       // first column of the pair
+  if (col >= p.cols) return;              // cols % 16 == 0: blocks are wholly in or out
+  const bool two = col + 16 < p.cols;     // the pair's second block exists
+  // 16-byte code stores and 16-bit scale stores when every pair is whole and aligned
+  const bool whole = (p.cols % 32) == 0 && ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(p.scales) & 1u) == 0);
+  const int64_t nb = p.cols / 16, kb = col / 16;
+  const int rl0 = tid >> 3;
+  int64_t r = r0 + rl0;
+  uint64_t q0 = ((uint64_t)r * (uint64_t)p.cols + (uint64_t)col) >> 1;  // pair index of element (r, col)
+  uint8_t* codes = p.codes + r * (p.cols / 2) + col / 2;
+  const uint64_t q_step = (uint64_t)p.cols * 8u;       // 16 rows of pairs
+  const int64_t c_step = p.cols * 8;                    // 16 rows of code bytes
+#pragma unroll 1
+  for (int i = 0; i < kColTileRows / 16; ++i, r += 16, q0 += q_step, codes += c_step) {
     if (r >= p.rows) break;
-    const uint4 a = *reinterpret_cast<const uint4*>(&tile[rl][8 * blk]);
-    const uint4 b = *reinterpret_cast<const uint4*>(&tile[rl][8 * blk + 4]);
-    float v[16];
-    unpack16(a, b, v);
-    float amax_b = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
-    const uint32_t sc = block_scale_code(amax_b, den);
-    const float enc = block_enc(sg, sc);
-    uint2 q;
-    if (kSR) {
-      const uint64_t q0 = ((uint64_t)r * (uint64_t)p.cols + (uint64_t)col) >> 1;
-      q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+    const int rl = rl0 + 16 * i;
+    const uint4 a0 = *reinterpret_cast<const uint4*>(&tile[rl][16 * bp]);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(&tile[rl][16 * bp + 4]);
+    const uint4 b0 = *reinterpret_cast<const uint4*>(&tile[rl][16 * bp + 8]);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(&tile[rl][16 * bp + 12]);
+    uint32_t sc0, sc1 = 0u;
+    const uint2 qa = rows_block<kSR>(p, enc_tab, a0, a1, den, q0, sc0);
+    uint2 qb = make_uint2(0u, 0u);
+    if (two) qb = rows_block<kSR>(p, enc_tab, b0, b1, den, q0 + 8u, sc1);
+    const int64_t so = kMMA ? mma_scale_offset(r, kb, nb / 4) : r * nb + kb;
+    if (whole) {
+      *reinterpret_cast<uint4*>(codes) = make_uint4(qa.x, qa.y, qb.x, qb.y);
+      *reinterpret_cast<uint16_t*>(p.scales + so) = (uint16_t)(sc0 | (sc1 << 8));
     } else {
-      q = encode16_rne(v, enc);
+      *reinterpret_cast<uint2*>(codes) = qa;
+      p.scales[so] = (uint8_t)sc0;
+      if (two) {
+        *reinterpret_cast<uint2*>(codes + 8) = qb;
+        p.scales[kMMA ? mma_scale_offset(r, kb + 1, nb / 4) : so + 1] = (uint8_t)sc1;
+      }
     }
-    *reinterpret_cast<uint2*>(p.codes + r * (p.cols / 2) + col / 2) = q;
-    const int64_t kb = col / 16;
-    p.scales[kMMA ? mma_scale_offset(r, kb, nb / 4) : r * nb + kb] = (uint8_t)sc;
   }
 }
 
@@ -483,9 +518,9 @@ __device__ __forceinline__ void rows_tile(const QuantParams& p, const uint32_t (
 // tile's scale is written on each of its 16 rows.  16 threads write 128
 // contiguous code bytes of a row.
 template <bool kSR, bool kMMA>
-__device__ __forceinline__ void rows2d_tile(const QuantParams& p,
+__device__ __forceinline__ void rows2d_tile(const QuantParams& p, const float* enc_tab,
                                             const uint32_t (&tile)[kColTileRows][kColTileCols / 2], int64_t r0,
-                                            int64_t c0, float sg, float den) {
+                                            int64_t c0, float den) {
   const int tid = threadIdx.x;
   const int h = tid & 1, tcol = (tid >> 1) & 15, trow = tid >> 5;
   const int64_t col = c0 + 16 * tcol;
@@ -501,7 +536,7 @@ __device__ __forceinline__ void rows2d_tile(const QuantParams& p,
   m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
   if (col >= p.cols || r0 + 16 * trow >= p.rows) return;  // whole 16x16 tiles only (rows, cols % 16 == 0)
   const uint32_t sc = block_scale_code(__uint_as_float(m), den);
-  const float enc = block_enc(sg, sc);
+  const float enc = enc_tab[sc];
   const int64_t nb = p.cols / 16, kb = col / 16;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
@@ -513,7 +548,7 @@ __device__ __forceinline__ void rows2d_tile(const QuantParams& p,
     uint2 q;
     if (kSR) {
       const uint64_t q0 = ((uint64_t)r * (uint64_t)p.cols + (uint64_t)col) >> 1;
-      q = encode16_sr(v, enc, mix32(p.sr_key ^ (uint32_t)(q0 >> 32)), q0);
+      q = encode16_sr(v, enc, pair_key(p, q0), q0);
     } else {
       q = encode16_rne(v, enc);
     }
@@ -525,15 +560,17 @@ __device__ __forceinline__ void rows2d_tile(const QuantParams& p,
 template <bool kSR, bool kMMA>
 __global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams p) {
   __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  __shared__ float enc_tab[128];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
+  fill_enc_table(enc_tab, sg);
   const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
   const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);
-    rows2d_tile<kSR, kMMA>(p, tile, tr * kColTileRows, tc * kColTileCols, sg, den);
+    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);  // its barrier also publishes enc_tab
+    rows2d_tile<kSR, kMMA>(p, enc_tab, tile, tr * kColTileRows, tc * kColTileCols, den);
     __syncthreads();
   }
 }
@@ -546,18 +583,21 @@ __global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams 
 template <bool kRowSR, bool kMMA>
 __global__ void __launch_bounds__(kColThreads, 6) quant_dual_kernel(QuantParams pr, QuantParams pc) {
   __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+  __shared__ float enc_r[128], enc_c[128];
   float amax_r, amax_c;
   const float sg_r = tensor_scale(pr, amax_r);
   const float sg_c = tensor_scale(pc, amax_c);
   const float den_r = __fmul_rn(sg_r, 6.0f), den_c = __fmul_rn(sg_c, 6.0f);
+  fill_enc_table(enc_r, sg_r);
+  fill_enc_table(enc_c, sg_c);
   const int64_t tiles_c = (pr.cols + kColTileCols - 1) / kColTileCols;
   const int64_t ntiles = ((pr.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
     const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
-    stage_tile(pr, tile, r0, c0);
-    rows_tile<kRowSR, kMMA>(pr, tile, r0, c0, sg_r, den_r);
-    cols_tile<true, true, false, kMMA>(pc, tile, r0, c0, sg_c, den_c);
+    stage_tile(pr, tile, r0, c0);  // its barrier also publishes the tables
+    rows_tile<kRowSR, kMMA>(pr, enc_r, tile, r0, c0, den_r);
+    cols_tile<true, true, false, kMMA>(pc, enc_c, tile, r0, c0, den_c);
     __syncthreads();
   }
 }
@@ -580,7 +620,7 @@ static int64_t resident_ctas(const void* kernel, int threads, const DeviceInfo& 
     // error is cleared, so the launch check that follows does not see it.
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-    if (e == cudaSuccess && fa.sharedSizeBytes > 0)
+    if (e == cudaSuccess && fa.sharedSizeBytes > 1024)
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) (void)cudaGetLastError();
@@ -600,6 +640,28 @@ static int grid_for(Kernel kernel, const DeviceInfo& dev, int64_t work_items, in
   return (int)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
+static int64_t tile_count(int64_t rows, int64_t cols) {
+  return ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
+}
+
+// Tile-staged amax pass: the plain amax into out_plain and/or the amax after
+// the column-wise transform into out_cols (null: not computed).
+static void launch_amax_tiles(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                              uint32_t signs, float* out_plain, float* out_cols, cudaStream_t s) {
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  const int64_t work = tile_count(rows, cols) * kColThreads;
+  if (out_plain && out_cols) {
+    auto k = amax_tile_kernel<true, true>;
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, out_plain, out_cols);
+  } else if (out_cols) {
+    auto k = amax_tile_kernel<false, true>;
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, nullptr, out_cols);
+  } else if (out_plain) {
+    auto k = amax_tile_kernel<true, false>;
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, out_plain, nullptr);
+  }
+}
+
 template <bool kSR, bool kRHT>
 static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
   const int64_t items = p.orows * (p.ocols / 16) / 2;  // two blocks per thread
@@ -614,8 +676,7 @@ static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma
 
 template <bool kSR>
 static void launch_rows_2d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
-  const int64_t tiles =
-      ((p.rows + kColTileRows - 1) / kColTileRows) * ((p.cols + kColTileCols - 1) / kColTileCols);
+  const int64_t tiles = tile_count(p.rows, p.cols);
   if (mma) {
     auto k = quant_rows_2d_kernel<kSR, true>;
     k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
@@ -627,8 +688,7 @@ static void launch_rows_2d(const DeviceInfo& dev, const QuantParams& p, bool mma
 
 template <bool kSR, bool kRHT, bool kTwoD>
 static void launch_cols(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
-  const int64_t tiles =
-      ((p.rows + kColTileRows - 1) / kColTileRows) * ((p.cols + kColTileCols - 1) / kColTileCols);
+  const int64_t tiles = tile_count(p.rows, p.cols);
   if (mma) {
     auto k = quant_cols_kernel<kSR, kRHT, kTwoD, true>;
     k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
@@ -636,6 +696,12 @@ static void launch_cols(const DeviceInfo& dev, const QuantParams& p, bool mma, c
     auto k = quant_cols_kernel<kSR, kRHT, kTwoD, false>;
     k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
   }
+}
+
+static void set_sr_keys(QuantParams& p, uint64_t sr_seed) {
+  const uint32_t key = stream_key(sr_seed, kTagSR);
+  p.sr_hk[0] = mix32(key);
+  p.sr_hk[1] = mix32(key ^ 1u);
 }
 
 int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
@@ -658,7 +724,7 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
   p.scales = out.scales;
   p.sg_out = out.global_scale;
   p.status = dev.status;
-  p.sr_key = stream_key(sr_seed, kTagSR);
+  set_sr_keys(p, sr_seed);
   p.rht_signs = signs;
 
   // Padding rows of the MMA scale layout read as zero.
@@ -681,8 +747,7 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
       amax_plain_kernel<<<grid_for(amax_plain_kernel, dev, rows * vpr, 256), 256, 0, stream>>>(
           reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out.amax);
     } else if (tr) {
-      amax_rht_cols_kernel<<<grid_for(amax_rht_cols_kernel, dev, (rows / 16) * (cols / 8), 256), 256, 0, stream>>>(
-          p.x, rows, cols, ld, signs, out.amax);
+      launch_amax_tiles(dev, x, rows, cols, ld, signs, nullptr, out.amax, stream);
     } else {
       amax_rht_rows_kernel<<<grid_for(amax_rht_rows_kernel, dev, rows * (cols / 16), 256), 256, 0, stream>>>(
           p.x, rows, cols, ld, signs, out.amax);
@@ -766,9 +831,11 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
     q->rht_signs = signs;
   }
   pr.orows = out_row.rows; pr.ocols = out_row.cols; pr.codes = out_row.codes; pr.scales = out_row.scales;
-  pr.sg_out = out_row.global_scale; pr.sr_key = stream_key(row_sr_seed, kTagSR);
+  pr.sg_out = out_row.global_scale;
+  set_sr_keys(pr, row_sr_seed);
   pc.orows = out_col.rows; pc.ocols = out_col.cols; pc.codes = out_col.codes; pc.scales = out_col.scales;
-  pc.sg_out = out_col.global_scale; pc.sr_key = stream_key(col_sr_seed, kTagSR);
+  pc.sg_out = out_col.global_scale;
+  set_sr_keys(pc, col_sr_seed);
   const bool mma = out_row.scale_layout == NVFP4_SCALES_MMA;  // the caller checks both layouts agree
 
   for (const nvfp4_tensor* o : {&out_row, &out_col}) {
@@ -777,12 +844,18 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
       if (cudaMemsetAsync(o->scales + (o->rows / 128) * band, 0, band, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     }
   }
-  // Pass 1: both amaxes from one read (unless both are supplied).
-  if (!(amax_row_in && amax_col_in)) {
-    if (cudaMemsetAsync(out_row.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (cudaMemsetAsync(out_col.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
-    amax_dual_kernel<<<grid_for(amax_dual_kernel, dev, (rows / 16) * (cols / 8), 256), 256, 0, stream>>>(
-        pr.x, rows, cols, ld, signs, out_row.amax, out_col.amax);
+  // Pass 1: the amaxes that were not supplied, from one read.  A supplied
+  // amax is never written here, so it may alias its operand's own amax.
+  if (!amax_row_in && cudaMemsetAsync(out_row.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (!amax_col_in && cudaMemsetAsync(out_col.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (!amax_row_in && !amax_col_in) {
+    launch_amax_tiles(dev, x, rows, cols, ld, signs, out_row.amax, out_col.amax, stream);
+  } else if (!amax_row_in) {
+    const int64_t vpr = cols / 8;
+    amax_plain_kernel<<<grid_for(amax_plain_kernel, dev, rows * vpr, 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out_row.amax);
+  } else if (!amax_col_in) {
+    launch_amax_tiles(dev, x, rows, cols, ld, signs, nullptr, out_col.amax, stream);
   }
   pr.amax_src = amax_row_in ? amax_row_in : out_row.amax;
   pr.amax_out = amax_row_in ? out_row.amax : nullptr;
@@ -790,7 +863,7 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
   pc.amax_out = amax_col_in ? out_col.amax : nullptr;
 
   // Pass 2: one read, both outputs.
-  const int64_t tiles = ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
+  const int64_t tiles = tile_count(rows, cols);
   if (row_sr) {
     if (mma) {
       auto k = quant_dual_kernel<true, true>;
@@ -812,17 +885,23 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
 }
 
 // ----------------------------------------------------- codec diagnostics --
+// The element encoders exactly as the quantisers run them, through both
+// lanes of a pair (even element: low nibble; odd element: high nibble); a
+// disagreement between the lanes is reported as 0xFF, which is never a code.
 __global__ void encode_e2m1_rne_kernel(const float* v, int64_t n, uint8_t* out) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const float a = v[i];
-    out[i] = (uint8_t)((e2m1x2_rne_mag(fabsf(a), 0.0f) & 0xFu) | sign_nibble(a));
+    const uint32_t lo = e2m1x2_rne(a, 0.0f) & 0xFu, hi = e2m1x2_rne(0.0f, a) >> 4;
+    out[i] = (uint8_t)(lo == hi ? lo : 0xFFu);
   }
 }
 
 __global__ void encode_e2m1_sr_kernel(const float* v, const uint16_t* u, int64_t n, uint8_t* out) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const float a = v[i];
-    out[i] = (uint8_t)(e2m1_sr_code(fabsf(a), (uint32_t)u[i] << 6) | sign_nibble(a));
+    const uint32_t r = (uint32_t)u[i];
+    const uint32_t lo = (sr_pair_b3(a, 0.0f, r) >> 24) & 0xFu, hi = sr_pair_b3(0.0f, a, r << 16) >> 28;
+    out[i] = (uint8_t)(lo == hi ? lo : 0xFFu);
   }
 }
 

@@ -109,6 +109,17 @@ def test_dual_and_mxfp4_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize_mxfp4(16, 4, 64, 68, 16, 16, None) == nv.ERR_INVALID_ARG
 
 
+def test_mma_rate_probe_arguments_rejected_on_host(lib):
+    pairs = ctypes.c_int32(0)
+    assert lib.nvfp4_mma_rate_probe(0, 256, 16, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_mma_rate_probe((1 << 20) + 1, 256, 16, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_mma_rate_probe(64, 192, 16, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_mma_rate_probe(64, 256, None, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_mma_rate_probe(64, 256, 12, ctypes.byref(pairs), None) == nv.ERR_INVALID_ARG  # misaligned
+    assert lib.nvfp4_mma_rate_probe(64, 256, 16, None, None) == nv.ERR_INVALID_ARG
+    assert pairs.value == 0
+
+
 def test_compute_calls_refuse_cpu_tensors():
     import torch
     x = torch.zeros(16, 16, dtype=torch.bfloat16)

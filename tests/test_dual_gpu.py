@@ -64,3 +64,28 @@ def test_dual_empty_and_rejects():
         nv.quantize_dual(y, nv.BLOCK_2D)          # 2D blocks are not a dual mode
     with pytest.raises(nv.Nvfp4Error):
         nv.quantize_dual(y[:, :200].contiguous())  # cols % 16 != 0 ... and % 64 for the MMA layout
+
+
+@pytest.mark.parametrize("supply", ["row", "col", "both"])
+def test_dual_with_supplied_amax_in_place(supply):
+    """A supplied amax may live in its own operand's amax buffer (the
+    single-pass mode of a caller that keeps the amax with the operand): the
+    call must neither clear it nor recompute it."""
+    rows, cols = 192, 512
+    x = make_bf16(TensorSpec(rows, cols, 1.0, 0.01, 40.0, 6), device="cuda")
+    rr, rc = _refs(x, True, 17, 18)
+    out_row = nv.empty_nvfp4(rows, cols, device="cuda")
+    out_col = nv.empty_nvfp4(cols, rows, device="cuda")
+    a_row = a_col = None
+    if supply in ("row", "both"):
+        out_row.amax.fill_(rr.amax)
+        a_row = out_row.amax
+    if supply in ("col", "both"):
+        out_col.amax.fill_(rc.amax)
+        a_col = out_col.amax
+    torch.cuda.synchronize()
+    nv.nvfp4_quantize_dual(x, nv.ROUND_SR, 17, RHT_SEED, 18, a_row, a_col, out_row, out_col)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.OK
+    assert_quant_equal(out_row, rr, "row")
+    assert_quant_equal(out_col, rc, "col")

@@ -16,7 +16,7 @@ import torch
 
 import nvfp4_block_scaled_27_b300 as nv
 import oracle as o
-from tests.helpers import assert_quant_equal, gemm_tolerance_check
+from tests.helpers import assert_quant_equal, sample_check
 from workloads import (LLAMA3_8B_DY, LLAMA3_8B_FPROP, LLAMA3_8B_W_BWD, LLAMA3_8B_X_BWD, LLAMA31_405B_FPROP,
                        RHT_SEED, bf16_bits, make_bf16, sr_seed, sweep_spec)
 
@@ -24,19 +24,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 def _sample_check(c, qa_h, qb_h, seed=0, n=4096, tile=128):
-    M, N = c.shape
-    rng = np.random.default_rng(seed)
-    mi = list(rng.integers(0, M, n))
-    ni = list(rng.integers(0, N, n))
-    for (r0, c0) in [(0, 0), (0, N - tile), (M - tile, 0), (M - tile, N - tile)]:
-        rr, cc = np.meshgrid(np.arange(r0, r0 + tile), np.arange(c0, c0 + tile), indexing="ij")
-        mi += list(rr.ravel())
-        ni += list(cc.ravel())
-    mi = np.array(mi, np.int64)
-    ni = np.array(ni, np.int64)
-    ref = o.gemm_sampled(qa_h, qb_h, mi, ni)
-    got = c[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].float().cpu().numpy().astype(np.float64)
-    gemm_tolerance_check(got, ref)
+    sample_check(c, qa_h, qb_h, seed=seed, n=n, tile=tile)
 
 
 def _quant_and_check(x, flags, rht=False, seed=0, what=""):

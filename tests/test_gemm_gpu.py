@@ -79,14 +79,17 @@ def test_unit_scale_structured_operands():
 
 
 def test_scale_layout_probe():
-    """Each row of A and each row of B gets its own power-of-two block scale
-    (distinct per 16-block), so any scale mix-up between rows, quadrants or
-    K-blocks changes the result."""
+    """Each row of A and each row of B gets its own block scale (a distinct
+    binade per 16-block), so any scale mix-up between rows, quadrants or
+    K-blocks changes the result.  Random mantissas in [1, 2) keep the
+    accumulator values varied, so outputs do not cluster on BF16 rounding
+    midpoints (equal power-of-two magnitudes would give a handful of distinct
+    sums, all on the same side of the same midpoints)."""
     M, N, K = 128, 256, 512
     g = torch.Generator(device="cuda").manual_seed(6)
-    a = torch.ones(M, K, device="cuda")
-    b = torch.ones(N, K, device="cuda")
-    # block (r, kb) amplitude 2^((r + kb) % 5 - 2); one element per block at 6x
+    a = 1.0 + torch.rand(M, K, generator=g, device="cuda")
+    b = 1.0 + torch.rand(N, K, generator=g, device="cuda")
+    # block (r, kb) of A spans the binade 2^((r + kb) % 5 - 2), random signs; B likewise
     ra = torch.arange(M, device="cuda")[:, None]
     rb = torch.arange(N, device="cuda")[:, None]
     kb = (torch.arange(K, device="cuda") // 16)[None, :]
@@ -206,3 +209,18 @@ def test_layout_pinned_by_cublaslt(M, N, K):
     ref = o.gemm(host_qtensor(qa), host_qtensor(qb))
     gemm_tolerance_check(lib.float().cpu().numpy().astype(np.float64), ref)
     gemm_tolerance_check(ours.float().cpu().numpy().astype(np.float64), ref)
+
+
+def test_mma_rate_probe_reports_every_pair():
+    """The FP4 MMA-rate probe (the GEMM roofline's measured denominator)
+    runs one CTA pair per two SMs and every pair reports a plausible time:
+    at least the 2 * 128 * 256 * 64 / 32768 = 128 cycles per pair MMA that
+    the tensor cores' measured dense NVFP4 rate allows, and not wildly more."""
+    nv.load_library()
+    r = nv.measure_mma_rate(2048, 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert r["pairs"] == sms // 2
+    assert 120.0 <= r["cycles_per_mma"] <= 400.0, r
+    assert 0.5 <= r["probe_sm_ghz"] <= 2.2, r
+    r128 = nv.measure_mma_rate(2048, 128)
+    assert r128["cycles_per_mma"] < r["cycles_per_mma"], (r128, r)
