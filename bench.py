@@ -824,8 +824,37 @@ def run_cases(args):
         ms = sorted(a.elapsed_time(b) for a, b in times)
         med = ms[len(ms) // 2]
         scale = 1e12 if unit == "TFLOP/s" else 1e9
-        print(json.dumps({"case": spec, "ms_median": round(med, 4), "ms_min": round(ms[0], 4),
-                          unit: round(work / (med * 1e-3) / scale, 1), "reps": args.steps}), flush=True)
+        rec = {"case": spec, "ms_median": round(med, 4), "ms_min": round(ms[0], 4),
+               unit: round(work / (med * 1e-3) / scale, 1), "reps": args.steps}
+        if args.b2b:
+            rec["sustained"] = _sustained(fn, stream, med, work, scale, unit)
+        print(json.dumps(rec), flush=True)
+
+
+def _sustained(fn, stream, ms_one, work, scale, unit, seconds=0.6):
+    """The same op back to back for about `seconds` (no flushes, no gaps)
+    with the SM clock sampled meanwhile: under the power cap a long run of a
+    tensor-bound kernel lowers the clock.  Reports the mean time per op, its
+    throughput, the median sampled SM clock and time x MHz (clock-normalised
+    cycles, comparable between runs at different clocks)."""
+    import nvfp4_block_scaled_27_b300 as nv
+    n = max(10, int(seconds * 1e3 / max(ms_one, 1e-3)))
+    time.sleep(0.5)  # idle first, so both runs start from the same clock state
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        stream.synchronize()
+    nv.check_status(stream)
+    ms = e0.elapsed_time(e1) / n
+    c = clk.summary()
+    out = {"launches": n, "ms_mean": round(ms, 4), unit: round(work / (ms * 1e-3) / scale, 1), "clocks": c}
+    if c.get("sm_mhz"):
+        out["ms_x_mhz"] = round(ms * c["sm_mhz"], 1)
+    return out
 
 
 def main():
@@ -839,6 +868,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="quantise-only sweep, 2^20 .. 2^30 elements")
     ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS BF16/FP8 context timings")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 2^30-element quantise-only point")
+    ap.add_argument("--b2b", action="store_true",
+                    help="with --case: also run each op back to back for ~0.6 s with clocks sampled")
     ap.add_argument("--case", action="append", default=[],
                     help="time single ops instead of the step: gemm:M,N,K or quant:MODE:ROWS,COLS")
     args = ap.parse_args()

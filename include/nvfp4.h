@@ -106,7 +106,12 @@ typedef struct nvfp4_tensor {
  * (0 for an invalid combination). */
 size_t nvfp4_scales_bytes(int64_t rows, int64_t cols, int32_t layout);
 
-/* Quantise a bf16 matrix x [rows, cols] (row stride ld elements) to NVFP4.
+/* Quantise a bf16 matrix x [rows, cols] (row stride ld elements) to NVFP4:
+ * E2M1 elements with one E4M3 scale per 16 values and one FP32 tensor scale
+ * ("NVFP4: cos'è e come supera FP8 e BF16 ...", section "Cos'è NVFP4 ...";
+ * "FP4" (chaitex.ru/fp4), section "Математическая структура FP4"), with the
+ * recipe's 16x16 weight blocks and stochastic rounding as options
+ * (readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph).
  * flags: NVFP4_BLOCK_1D or NVFP4_BLOCK_2D, NVFP4_ROUND_RNE or NVFP4_ROUND_SR,
  * optionally NVFP4_TRANSPOSE_OUT (then out is [cols, rows], blocks run along
  * the input's rows).  out->rows/out->cols must equal the output shape.
@@ -120,7 +125,10 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
                    const nvfp4_tensor* out, nvfp4_stream_t stream);
 
 /* Quantise with the 16-point random Hadamard transform and stochastic
- * rounding (the wgrad operands).  The transform runs along the output's
+ * rounding: the recipe's treatment of the wgrad operands (readjensen.com
+ * NVFP4 training-recipe article, MLP data-flow paragraph: a random Hadamard
+ * transform before 4-bit quantisation of the weight-gradient inputs,
+ * stochastic rounding for gradients).  The transform runs along the output's
  * quantisation axis, so with NVFP4_TRANSPOSE_OUT (the usual wgrad case) it
  * mixes 16 consecutive rows (tokens) of x.  Both wgrad operands must use the
  * same rht_seed; use different sr_seeds.  The amax is taken after the
@@ -173,7 +181,12 @@ int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, 
                          uint8_t* scales_e8m0, nvfp4_stream_t stream);
 
 /* Block-scaled NVFP4 GEMM, "TN": C[M, N] = s_gA * s_gB * A[M, K] * B[N, K]^T
- * with fp32 accumulation and a BF16 (round-to-nearest-even) result.
+ * with fp32 accumulation and a BF16 (round-to-nearest-even) result: the
+ * recipe's three MLP GEMMs take NVFP4 operands and return BF16
+ * (readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph),
+ * and the fifth-generation tensor cores apply the block scales in hardware
+ * ("NVFP4: cos'è e come supera FP8 e BF16 ...", section "Blackwell
+ * Architecture: la potenza dietro NVFP4").
  * A and B must use NVFP4_SCALES_MMA, K = A->cols = B->cols, K % 256 == 0.
  * c is bf16 [M, N] with row stride ldc elements (ldc >= N, ldc % 8 == 0,
  * c 16-byte aligned).  The same call serves fprop (X * W^T), dgrad

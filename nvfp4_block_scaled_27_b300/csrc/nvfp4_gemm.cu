@@ -36,10 +36,12 @@
 //               and arrive on the leader's `sf_done`.  (tcgen05.cp of the
 //               same data stalls the MMA stream.)
 //   warps 7-14  epilogue: two warps per lane quadrant each pull 128 fp32
-//               columns out of tensor memory, scale by s_gA * s_gB and round
-//               to packed BF16 in registers, release the accumulator to the
-//               leader (the next tile's MMAs start), then write 32 x 32 BF16
-//               boxes through swizzled shared memory with TMA stores.
+//               columns out of tensor memory in two halves, scale by
+//               s_gA * s_gB (packed pairs) and round to packed BF16 in
+//               registers; the accumulator is released to the leader as soon
+//               as the second half is in registers (the next tile's MMAs
+//               start while it is converted), then 32 x 32 BF16 boxes go out
+//               through swizzled shared memory with TMA stores.
 // The refill of a stage thus waits only on the operand copies; scales are
 // written off that path.  Tensor memory (512 columns, same addresses in both
 // CTAs): accumulator [0, 256) + per-stage scale columns (SFA 4 x 4, SFB 4 x 8).
@@ -115,12 +117,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
 }
 
-// Two accumulator values scaled by alpha and rounded to BF16 (nearest even),
-// packed with `lo` in the low half-word.  The product is rounded to fp32
-// first; the result differs from rounding the exact product only when that
-// fp32 value sits exactly on a BF16 tie.
-__device__ __forceinline__ uint32_t scale_pack_bf16x2(float lo, float hi, float alpha) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lo, alpha), __fmul_rn(hi, alpha));
+// Two accumulator values (fp32 bit patterns) scaled by alpha and rounded to
+// BF16 (nearest even), packed with `lo` in the low half-word.  The packed
+// multiply rounds each lane like the scalar one; the product is rounded to
+// fp32 first, and the result differs from rounding the exact product only
+// when that fp32 value sits exactly on a BF16 tie.
+__device__ __forceinline__ uint32_t scale_pack2(uint32_t lo, uint32_t hi, uint64_t alpha2) {
+  float a, b;
+  f2_unpack(f2_mul(f2_pack(__uint_as_float(lo), __uint_as_float(hi)), alpha2), a, b);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
@@ -370,6 +375,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     const int quad = warp & 3;                     // lane quadrant this warp may access
     const int half = (warp - FIRST_EPI_WARP) >> 2;  // which 128 accumulator columns
     const float alpha = __fmul_rn(*p.sga, *p.sgb);
+    const uint64_t alpha2 = f2_pack(alpha, alpha);
     const uint32_t leader_tmem_empty = mapa_shared(bar_tmem_empty, 0);
     const uint32_t stage_buf = sbase + OFF_EPI + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * EPI_BUF_BYTES);
     const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
@@ -389,21 +395,30 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       // bf16x2 words; release the accumulator as soon as the last chunk is
       // in registers so the next tile's MMAs overlap the stores.
       uint32_t w[64];
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {  // two loads in flight per wait
+      {
         uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(taddr + 64 * pr, v0);
-        tmem_ld_32x32b_x32(taddr + 64 * pr + 32, v1);
+        tmem_ld_32x32b_x32(taddr, v0);
+        tmem_ld_32x32b_x32(taddr + 32, v1);
         tc_wait_ld();
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          w[32 * pr + q] = scale_pack_bf16x2(__uint_as_float(v0[2 * q]), __uint_as_float(v0[2 * q + 1]), alpha);
-          w[32 * pr + 16 + q] = scale_pack_bf16x2(__uint_as_float(v1[2 * q]), __uint_as_float(v1[2 * q + 1]), alpha);
+          w[q] = scale_pack2(v0[2 * q], v0[2 * q + 1], alpha2);
+          w[16 + q] = scale_pack2(v1[2 * q], v1[2 * q + 1], alpha2);
+        }
+        tmem_ld_32x32b_x32(taddr + 64, v0);
+        tmem_ld_32x32b_x32(taddr + 96, v1);
+        tc_wait_ld();
+        // every accumulator column this warp reads is in registers: release
+        // the accumulator before converting the second half
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          w[32 + q] = scale_pack2(v0[2 * q], v0[2 * q + 1], alpha2);
+          w[48 + q] = scale_pack2(v1[2 * q], v1[2 * q + 1], alpha2);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
       const int row0 = tm * BM_PAIR + (int)rank * BM + quad * 32;
       const int col0 = tn * BN + half * 128;
       if (row0 >= p.M) continue;
@@ -568,6 +583,22 @@ static bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int6
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map over a bf16 matrix [rows, cols] (row stride ld elements) with boxes of
+// box_cols x box_rows elements, no swizzle; elements outside the matrix read
+// as zero.  The quantisers stage their input tiles through it.
+bool make_bf16_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                        int box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

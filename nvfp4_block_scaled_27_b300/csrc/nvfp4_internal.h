@@ -2,6 +2,7 @@
 // units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,6 +20,11 @@ struct DeviceInfo {
 
 // Current device's info (filled once per device); nullptr on failure.
 const DeviceInfo* device_info();
+
+// TMA map over a bf16 matrix [rows, cols] (row stride ld elements) with
+// box_cols x box_rows boxes, zero fill outside; false on failure.
+bool make_bf16_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                        int box_rows);
 
 // Quantiser entry used by both public quantise calls.  Arguments have been
 // validated by the caller.

@@ -207,32 +207,56 @@ constexpr int kColTileRows = 64;   // input rows per tile (4 blocks)
 constexpr int kColTileCols = 256;  // input columns per tile
 constexpr int kColThreads = 128;   // one thread per column pair
 
-// Stage the tile (r0, c0) of the input in shared memory with asynchronous
-// 16-byte copies (all of a thread's copies in flight at once, no registers
-// held); a warp moves one 512-byte input row segment per step and elements
-// outside the input are zero-filled.  Ends with the copies complete and the
-// tile visible to the whole CTA.
-__device__ __forceinline__ void stage_tile(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                                           uint32_t (&tile)[kColTileRows][kColTileCols / 2], int64_t r0,
-                                           int64_t c0) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int k = 0; k < (kColTileRows * kColTileCols / 8) / kColThreads; ++k) {
-    const int idx = k * kColThreads + tid;
-    const int row = idx / (kColTileCols / 8), vec = idx % (kColTileCols / 8);
-    const bool ok = r0 + row < rows && c0 + vec * 8 < cols;
-    const uint16_t* src = ok ? x + (r0 + row) * ld + c0 + vec * 8 : x;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(&tile[row][vec * 4])), "l"(src),
-                 "r"(ok ? 16 : 0)
-                 : "memory");
+constexpr uint32_t kTileBytes = kColTileRows * kColTileCols * 2;
+
+// Shared memory of a tile-staged kernel: the input tile (the TMA box,
+// row-major, 512 bytes per row) and the mbarrier its copy completes on.
+struct TileSmem {
+  __align__(128) uint32_t tile[kColTileRows][kColTileCols / 2];
+  __align__(8) uint64_t bar;
+};
+
+// Walks the input's 64 x 256 tiles (forwards, or backwards with kReverse)
+// with a grid stride; each tile arrives in shared memory by one TMA copy
+// that thread 0 issues and every thread waits for (elements outside the
+// input read as zero), then body(r0, c0) runs on it.  One barrier per tile
+// separates the body's reads from the next copy; a wait that expires (the
+// timeout bit is then raised) ends the walk for the whole CTA.  The caller
+// initialises ts.bar and synchronises before the first call.
+template <bool kReverse, typename Body>
+__device__ __forceinline__ void for_each_tile(const CUtensorMap& map, TileSmem& ts, int64_t rows, int64_t cols,
+                                              uint32_t* status, Body&& body) {
+  const int64_t tiles_c = (cols + kColTileCols - 1) / kColTileCols;
+  const int64_t ntiles = ((rows + kColTileRows - 1) / kColTileRows) * tiles_c;
+  const int64_t step = kReverse ? -(int64_t)gridDim.x : (int64_t)gridDim.x;
+  int64_t t = kReverse ? ntiles - 1 - blockIdx.x : blockIdx.x;
+  if (t < 0 || t >= ntiles) return;
+  const uint32_t bar = smem_u32(&ts.bar), dst = smem_u32(&ts.tile[0][0]);
+  auto issue = [&](int64_t tt) {
+    const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
+    fence_proxy_async();  // earlier generic reads of the tile before the async-proxy write
+    mbar_arrive_expect_tx(bar, kTileBytes);
+    tma_load_2d(dst, &map, (int32_t)(tc * kColTileCols), (int32_t)(tr * kColTileRows), bar);
+  };
+  if (threadIdx.x == 0) issue(t);
+  uint32_t phase = 0u;
+  while (true) {
+    const bool ok = mbar_wait(bar, phase, status);
+    phase ^= 1u;
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    body(tr * kColTileRows, tc * kColTileCols);
+    const int64_t tn = t + step;
+    if (__syncthreads_or(!ok) || tn < 0 || tn >= ntiles) break;
+    t = tn;
+    if (threadIdx.x == 0) issue(t);
   }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
 }
 
-__device__ __forceinline__ void stage_tile(const QuantParams& p, uint32_t (&tile)[kColTileRows][kColTileCols / 2],
-                                           int64_t r0, int64_t c0) {
-  stage_tile(p.x, p.rows, p.cols, p.ld, tile, r0, c0);
+__device__ __forceinline__ void tile_smem_init(TileSmem& ts) {
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ts.bar), 1);
+    fence_barrier_init();
+  }
 }
 
 // The 32 values of a thread's column pair in one 16-row chunk of a staged
@@ -253,32 +277,29 @@ __device__ __forceinline__ void load_chunk_cols(const uint32_t (&tile)[kColTileR
 // consecutive rows of a column, 1/4 applied once at the end).  Zero-filled
 // padding does not change either maximum.
 template <bool kPlain, bool kCols>
-__global__ void __launch_bounds__(kColThreads) amax_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                                int64_t cols, int64_t ld, uint32_t signs,
-                                                                float* out_plain, float* out_cols) {
-  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+__global__ void __launch_bounds__(kColThreads) amax_tile_kernel(const __grid_constant__ CUtensorMap map, int64_t rows,
+                                                                int64_t cols, uint32_t signs, float* out_plain,
+                                                                float* out_cols, uint32_t* status) {
+  __shared__ TileSmem ts;
+  tile_smem_init(ts);
+  __syncthreads();
   uint32_t mp = 0u;
   float mc = 0.0f;
-  const int64_t tiles_c = (cols + kColTileCols - 1) / kColTileCols;
-  const int64_t ntiles = ((rows + kColTileRows - 1) / kColTileRows) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    stage_tile(x, rows, cols, ld, tile, tr * kColTileRows, tc * kColTileCols);
+  for_each_tile<false>(map, ts, rows, cols, status, [&](int64_t, int64_t) {
 #pragma unroll 1
     for (int k = 0; k < kColTileRows / 16; ++k) {
       if (kPlain) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) mp = __vmaxu2(mp, tile[16 * k + i][threadIdx.x] & 0x7FFF7FFFu);
+        for (int i = 0; i < 16; ++i) mp = __vmaxu2(mp, ts.tile[16 * k + i][threadIdx.x] & 0x7FFF7FFFu);
       }
       if (kCols) {
         float v0[16], v1[16];
-        load_chunk_cols(tile, k, v0, v1);
+        load_chunk_cols(ts.tile, k, v0, v1);
         rht16x2_unscaled(v0, v1, signs);
         mc = absmax3(mc, absmax16(v0), absmax16(v1));
       }
     }
-    __syncthreads();
-  }
+  });
   cta_amax_commit2(pairs_to_f32_bits(mp), kPlain ? out_plain : nullptr, __float_as_uint(__fmul_rn(mc, 0.25f)),
                    kCols ? out_cols : nullptr);
 }
@@ -434,21 +455,21 @@ __device__ __forceinline__ void cols_tile(const QuantParams& p, const float* enc
 }
 
 template <bool kSR, bool kRHT, bool kTwoD, bool kMMA>
-__global__ void __launch_bounds__(kColThreads, 6) quant_cols_kernel(QuantParams p) {
-  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+__global__ void __launch_bounds__(kColThreads, 6) quant_cols_kernel(const __grid_constant__ CUtensorMap map,
+                                                                    QuantParams p) {
+  __shared__ TileSmem ts;
   __shared__ float enc_tab[128];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
   fill_enc_table(enc_tab, sg);
-  const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
-  const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);  // its barrier also publishes enc_tab
-    cols_tile<kSR, kRHT, kTwoD, kMMA>(p, enc_tab, tile, tr * kColTileRows, tc * kColTileCols, den);
-    __syncthreads();
-  }
+  tile_smem_init(ts);
+  __syncthreads();
+  // Tiles in reverse order: the amax pass walked them forwards, so the first
+  // tiles encoded are the ones it left in L2.
+  for_each_tile<true>(map, ts, p.rows, p.cols, p.status, [&](int64_t r0, int64_t c0) {
+    cols_tile<kSR, kRHT, kTwoD, kMMA>(p, enc_tab, ts.tile, r0, c0, den);
+  });
 }
 
 // Row-wise 1D quantisation of a staged tile: thread t owns the two
@@ -558,21 +579,38 @@ __device__ __forceinline__ void rows2d_tile(const QuantParams& p, const float* e
 }
 
 template <bool kSR, bool kMMA>
-__global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams p) {
-  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+__global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(const __grid_constant__ CUtensorMap map,
+                                                                   QuantParams p) {
+  __shared__ TileSmem ts;
   __shared__ float enc_tab[128];
   float amax;
   const float sg = tensor_scale(p, amax);
   const float den = __fmul_rn(sg, 6.0f);
   fill_enc_table(enc_tab, sg);
-  const int64_t tiles_c = (p.cols + kColTileCols - 1) / kColTileCols;
-  const int64_t ntiles = ((p.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    stage_tile(p, tile, tr * kColTileRows, tc * kColTileCols);  // its barrier also publishes enc_tab
-    rows2d_tile<kSR, kMMA>(p, enc_tab, tile, tr * kColTileRows, tc * kColTileCols, den);
-    __syncthreads();
-  }
+  tile_smem_init(ts);
+  __syncthreads();
+  for_each_tile<true>(map, ts, p.rows, p.cols, p.status, [&](int64_t r0, int64_t c0) {
+    rows2d_tile<kSR, kMMA>(p, enc_tab, ts.tile, r0, c0, den);
+  });
+}
+
+// Row-wise 1D quantisation through staged tiles (no transform): the tile's
+// copies are asynchronous, so a CTA keeps a whole 32 KiB tile in flight
+// without holding registers, and six CTAs per SM cover DRAM latency.
+template <bool kSR, bool kMMA>
+__global__ void __launch_bounds__(kColThreads, 6) quant_rows_tile_kernel(const __grid_constant__ CUtensorMap map,
+                                                                         QuantParams p) {
+  __shared__ TileSmem ts;
+  __shared__ float enc_tab[128];
+  float amax;
+  const float sg = tensor_scale(p, amax);
+  const float den = __fmul_rn(sg, 6.0f);
+  fill_enc_table(enc_tab, sg);
+  tile_smem_init(ts);
+  __syncthreads();
+  for_each_tile<true>(map, ts, p.rows, p.cols, p.status, [&](int64_t r0, int64_t c0) {
+    rows_tile<kSR, kMMA>(p, enc_tab, ts.tile, r0, c0, den);
+  });
 }
 
 // Dual-orientation quantisation: one read of each input tile produces the
@@ -581,8 +619,9 @@ __global__ void __launch_bounds__(kColThreads) quant_rows_2d_kernel(QuantParams 
 // Six CTAs per SM (80 registers, 6 x 32 KiB tiles): the encodes are bound
 // by instruction issue, and more resident warps hide their latencies.
 template <bool kRowSR, bool kMMA>
-__global__ void __launch_bounds__(kColThreads, 6) quant_dual_kernel(QuantParams pr, QuantParams pc) {
-  __shared__ __align__(16) uint32_t tile[kColTileRows][kColTileCols / 2];
+__global__ void __launch_bounds__(kColThreads, 6) quant_dual_kernel(const __grid_constant__ CUtensorMap map,
+                                                                    QuantParams pr, QuantParams pc) {
+  __shared__ TileSmem ts;
   __shared__ float enc_r[128], enc_c[128];
   float amax_r, amax_c;
   const float sg_r = tensor_scale(pr, amax_r);
@@ -590,16 +629,12 @@ __global__ void __launch_bounds__(kColThreads, 6) quant_dual_kernel(QuantParams 
   const float den_r = __fmul_rn(sg_r, 6.0f), den_c = __fmul_rn(sg_c, 6.0f);
   fill_enc_table(enc_r, sg_r);
   fill_enc_table(enc_c, sg_c);
-  const int64_t tiles_c = (pr.cols + kColTileCols - 1) / kColTileCols;
-  const int64_t ntiles = ((pr.rows + kColTileRows - 1) / kColTileRows) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
-    const int64_t r0 = tr * kColTileRows, c0 = tc * kColTileCols;
-    stage_tile(pr, tile, r0, c0);  // its barrier also publishes the tables
-    rows_tile<kRowSR, kMMA>(pr, enc_r, tile, r0, c0, den_r);
-    cols_tile<true, true, false, kMMA>(pc, enc_c, tile, r0, c0, den_c);
-    __syncthreads();
-  }
+  tile_smem_init(ts);
+  __syncthreads();
+  for_each_tile<true>(map, ts, pr.rows, pr.cols, pr.status, [&](int64_t r0, int64_t c0) {
+    rows_tile<kRowSR, kMMA>(pr, enc_r, ts.tile, r0, c0, den_r);
+    cols_tile<true, true, false, kMMA>(pc, enc_c, ts.tile, r0, c0, den_c);
+  });
 }
 
 // ------------------------------------------------------------- launch --
@@ -644,26 +679,49 @@ static int64_t tile_count(int64_t rows, int64_t cols) {
   return ((rows + kColTileRows - 1) / kColTileRows) * ((cols + kColTileCols - 1) / kColTileCols);
 }
 
+// TMA map of the input as 64 x 256 tiles.
+static bool input_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols, int64_t ld) {
+  return make_bf16_tile_map(m, x, rows, cols, ld, kColTileCols, kColTileRows);
+}
+
 // Tile-staged amax pass: the plain amax into out_plain and/or the amax after
 // the column-wise transform into out_cols (null: not computed).
-static void launch_amax_tiles(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld,
+static void launch_amax_tiles(const DeviceInfo& dev, const CUtensorMap& map, int64_t rows, int64_t cols,
                               uint32_t signs, float* out_plain, float* out_cols, cudaStream_t s) {
-  const uint16_t* xs = static_cast<const uint16_t*>(x);
   const int64_t work = tile_count(rows, cols) * kColThreads;
   if (out_plain && out_cols) {
     auto k = amax_tile_kernel<true, true>;
-    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, out_plain, out_cols);
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(map, rows, cols, signs, out_plain, out_cols,
+                                                                   dev.status);
   } else if (out_cols) {
     auto k = amax_tile_kernel<false, true>;
-    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, nullptr, out_cols);
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(map, rows, cols, signs, nullptr, out_cols,
+                                                                   dev.status);
   } else if (out_plain) {
     auto k = amax_tile_kernel<true, false>;
-    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(xs, rows, cols, ld, signs, out_plain, nullptr);
+    k<<<grid_for(k, dev, work, kColThreads), kColThreads, 0, s>>>(map, rows, cols, signs, out_plain, nullptr,
+                                                                   dev.status);
   }
 }
 
 template <bool kSR, bool kRHT>
-static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+static void launch_rows_1d(const DeviceInfo& dev, const CUtensorMap& map, const QuantParams& p, bool mma,
+                           cudaStream_t s) {
+  // Round-to-nearest rows go through staged tiles (HBM-bound: the TMA keeps
+  // a whole tile in flight per CTA); stochastic rounding and the row-wise
+  // transform keep the register-resident kernel, which measured faster for
+  // those instruction-bound modes.
+  if constexpr (!kRHT && !kSR) {
+    const int64_t tiles = tile_count(p.rows, p.cols);
+    if (mma) {
+      auto k = quant_rows_tile_kernel<kSR, true>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
+    } else {
+      auto k = quant_rows_tile_kernel<kSR, false>;
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
+    }
+    return;
+  }
   const int64_t items = p.orows * (p.ocols / 16) / 2;  // two blocks per thread
   if (mma) {
     auto k = quant_rows_1d_kernel<kSR, kRHT, true>;
@@ -675,26 +733,28 @@ static void launch_rows_1d(const DeviceInfo& dev, const QuantParams& p, bool mma
 }
 
 template <bool kSR>
-static void launch_rows_2d(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+static void launch_rows_2d(const DeviceInfo& dev, const CUtensorMap& map, const QuantParams& p, bool mma,
+                           cudaStream_t s) {
   const int64_t tiles = tile_count(p.rows, p.cols);
   if (mma) {
     auto k = quant_rows_2d_kernel<kSR, true>;
-    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
   } else {
     auto k = quant_rows_2d_kernel<kSR, false>;
-    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
   }
 }
 
 template <bool kSR, bool kRHT, bool kTwoD>
-static void launch_cols(const DeviceInfo& dev, const QuantParams& p, bool mma, cudaStream_t s) {
+static void launch_cols(const DeviceInfo& dev, const CUtensorMap& map, const QuantParams& p, bool mma,
+                        cudaStream_t s) {
   const int64_t tiles = tile_count(p.rows, p.cols);
   if (mma) {
     auto k = quant_cols_kernel<kSR, kRHT, kTwoD, true>;
-    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
   } else {
     auto k = quant_cols_kernel<kSR, kRHT, kTwoD, false>;
-    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(p);
+    k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, s>>>(map, p);
   }
 }
 
@@ -734,6 +794,9 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
       return NVFP4_ERR_CUDA;
   }
 
+  CUtensorMap map;
+  if (!input_map(&map, x, rows, cols, ld)) return NVFP4_ERR_CUDA;
+
   // Pass 1: tensor amax (unless supplied).
   if (amax_in) {
     p.amax_src = amax_in;
@@ -747,7 +810,7 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
       amax_plain_kernel<<<grid_for(amax_plain_kernel, dev, rows * vpr, 256), 256, 0, stream>>>(
           reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out.amax);
     } else if (tr) {
-      launch_amax_tiles(dev, x, rows, cols, ld, signs, nullptr, out.amax, stream);
+      launch_amax_tiles(dev, map, rows, cols, signs, nullptr, out.amax, stream);
     } else {
       amax_rht_rows_kernel<<<grid_for(amax_rht_rows_kernel, dev, rows * (cols / 16), 256), 256, 0, stream>>>(
           p.x, rows, cols, ld, signs, out.amax);
@@ -757,24 +820,24 @@ int quantize_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t 
   // Pass 2: scales and codes.
   if (!tr) {
     if (two_d) {
-      if (sr) launch_rows_2d<true>(dev, p, mma, stream);
-      else launch_rows_2d<false>(dev, p, mma, stream);
+      if (sr) launch_rows_2d<true>(dev, map, p, mma, stream);
+      else launch_rows_2d<false>(dev, map, p, mma, stream);
     } else {
-      if (sr && rht) launch_rows_1d<true, true>(dev, p, mma, stream);
-      else if (sr) launch_rows_1d<true, false>(dev, p, mma, stream);
-      else if (rht) launch_rows_1d<false, true>(dev, p, mma, stream);
-      else launch_rows_1d<false, false>(dev, p, mma, stream);
+      if (sr && rht) launch_rows_1d<true, true>(dev, map, p, mma, stream);
+      else if (sr) launch_rows_1d<true, false>(dev, map, p, mma, stream);
+      else if (rht) launch_rows_1d<false, true>(dev, map, p, mma, stream);
+      else launch_rows_1d<false, false>(dev, map, p, mma, stream);
     }
   } else {
     if (two_d) {
-      if (sr) launch_cols<true, false, true>(dev, p, mma, stream);
-      else launch_cols<false, false, true>(dev, p, mma, stream);
+      if (sr) launch_cols<true, false, true>(dev, map, p, mma, stream);
+      else launch_cols<false, false, true>(dev, map, p, mma, stream);
     } else if (rht) {
-      launch_cols<true, true, false>(dev, p, mma, stream);
+      launch_cols<true, true, false>(dev, map, p, mma, stream);
     } else if (sr) {
-      launch_cols<true, false, false>(dev, p, mma, stream);
+      launch_cols<true, false, false>(dev, map, p, mma, stream);
     } else {
-      launch_cols<false, false, false>(dev, p, mma, stream);
+      launch_cols<false, false, false>(dev, map, p, mma, stream);
     }
   }
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
@@ -844,18 +907,20 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
       if (cudaMemsetAsync(o->scales + (o->rows / 128) * band, 0, band, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     }
   }
+  CUtensorMap map;
+  if (!input_map(&map, x, rows, cols, ld)) return NVFP4_ERR_CUDA;
   // Pass 1: the amaxes that were not supplied, from one read.  A supplied
   // amax is never written here, so it may alias its operand's own amax.
   if (!amax_row_in && cudaMemsetAsync(out_row.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (!amax_col_in && cudaMemsetAsync(out_col.amax, 0, sizeof(float), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (!amax_row_in && !amax_col_in) {
-    launch_amax_tiles(dev, x, rows, cols, ld, signs, out_row.amax, out_col.amax, stream);
+    launch_amax_tiles(dev, map, rows, cols, signs, out_row.amax, out_col.amax, stream);
   } else if (!amax_row_in) {
     const int64_t vpr = cols / 8;
     amax_plain_kernel<<<grid_for(amax_plain_kernel, dev, rows * vpr, 256), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(x), rows, vpr, ld / 8, out_row.amax);
   } else if (!amax_col_in) {
-    launch_amax_tiles(dev, x, rows, cols, ld, signs, nullptr, out_col.amax, stream);
+    launch_amax_tiles(dev, map, rows, cols, signs, nullptr, out_col.amax, stream);
   }
   pr.amax_src = amax_row_in ? amax_row_in : out_row.amax;
   pr.amax_out = amax_row_in ? out_row.amax : nullptr;
@@ -867,18 +932,18 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
   if (row_sr) {
     if (mma) {
       auto k = quant_dual_kernel<true, true>;
-      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(map, pr, pc);
     } else {
       auto k = quant_dual_kernel<true, false>;
-      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(map, pr, pc);
     }
   } else {
     if (mma) {
       auto k = quant_dual_kernel<false, true>;
-      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(map, pr, pc);
     } else {
       auto k = quant_dual_kernel<false, false>;
-      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(pr, pc);
+      k<<<grid_for(k, dev, tiles * kColThreads, kColThreads), kColThreads, 0, stream>>>(map, pr, pc);
     }
   }
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
