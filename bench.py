@@ -640,12 +640,18 @@ def run_sweep(args):
         o_row = nv.empty_nvfp4(R, C, device=dev)
         o_col = nv.empty_nvfp4(C, R, device=dev)
         torch.cuda.synchronize()  # inputs were made on the default stream; the timed calls run on `stream`
+        nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(3), None, o_col, stream)
+        stream.synchronize()
+        ain_rht = o_col.amax.clone()  # the amax after the transform, for the single-pass RHT mode
         modes = {
             "1d_rne": lambda: nv.nvfp4_quantize(x, nv.BLOCK_1D, 0, None, o_row, stream),
             "1d_rne_amax_supplied": lambda: nv.nvfp4_quantize(x, nv.BLOCK_1D, 0, ain, o_row, stream),
             "2d": lambda: nv.nvfp4_quantize(x, nv.BLOCK_2D, 0, None, o_row, stream),
+            "2d_amax_supplied": lambda: nv.nvfp4_quantize(x, nv.BLOCK_2D, 0, ain, o_row, stream),
             "rht_sr_transposed": lambda: nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED, sr_seed(3), None,
                                                                   o_col, stream),
+            "rht_sr_transposed_amax_supplied": lambda: nv.nvfp4_quantize_rht_sr(x, nv.TRANSPOSE_OUT, RHT_SEED,
+                                                                                sr_seed(3), ain_rht, o_col, stream),
         }
         for name, fn in modes.items():
             with torch.cuda.stream(stream):
@@ -666,7 +672,7 @@ def run_sweep(args):
             print(json.dumps({"sweep": f"2^{lg}", "rows": R, "cols": C, "mode": name, "ms_median": round(ms, 4),
                               "gbs_algorithmic": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}),
                   flush=True)
-        del x, o_row, o_col
+        del x, o_row, o_col, ain_rht
 
 
 # ---------------------------------------------------- library context --
