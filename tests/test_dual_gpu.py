@@ -89,3 +89,19 @@ def test_dual_with_supplied_amax_in_place(supply):
     assert nv.nvfp4_check_status() == nv.OK
     assert_quant_equal(out_row, rr, "row")
     assert_quant_equal(out_col, rc, "col")
+
+
+@pytest.mark.parametrize("row_sr", [False, True])
+def test_dual_strided_and_ragged_input(row_sr):
+    """A column slice of a wider matrix (row stride 640 elements, 16-byte
+    aligned start) with rows that do not fill the last 64-row tile: both
+    operands equal the oracle's separate quantisations."""
+    base = make_bf16(TensorSpec(208, 640, 1.0, 0.01, 40.0, 9), device="cuda")
+    x = base[:, 64:576]  # [208, 512], ld = 640
+    q_row, q_col = nv.quantize_dual(x, nv.ROUND_SR if row_sr else 0, row_sr_seed=21, rht_seed=RHT_SEED,
+                                    col_sr_seed=22, layout=nv.SCALES_CANONICAL)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_check_status() == nv.OK
+    rr, rc = _refs(x, row_sr, 21, 22)
+    assert_quant_equal(q_row, rr, "row")
+    assert_quant_equal(q_col, rc, "col")
