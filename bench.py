@@ -264,6 +264,7 @@ def run_ours(args):
         probe = mma_probe(nv, clocks)
         qroof = quant_roofline(nv, step, stream, peaks, args)
         sweep = sweep_point(nv, stream, peaks, args) if not args.no_sweep else None
+    graph = graph_replay(step, stream, args) if not args.no_graph else None
     e2e = run_e2e(nv, step, stream, device, args) if rank == 0 and not args.no_e2e else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
     context = cublas_context(device) if (rank == 0 and not args.no_context) else None
@@ -314,6 +315,7 @@ def run_ours(args):
             "quantize_gbs_all": round(quant_gbs, 1),
             "quantize_ms_all": round(sum(quant_ms), 4),
             "roofline": roofline,
+            "graph": graph,
             "quant_roofline": qroof,
             "quant_sweep_2e30": sweep,
             "cpu_baseline": cpu,
@@ -357,6 +359,40 @@ def _event_ms(fn, stream, reps, warmup=2, flush=None):
     stream.synchronize()
     t = sorted(a.elapsed_time(b) for a, b in ev)
     return t[len(t) // 2]
+
+
+def graph_replay(step, stream, args):
+    """The same step captured once in a CUDA graph and replayed K times
+    (launch work done once at capture): its time per step, and whether the
+    replayed outputs equal the eager step's bit for bit (every input and
+    seed is the same each step, so they must)."""
+    try:
+        eager = [t.clone() for t in (step.y, step.dx, step.dw)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run(stream)
+        torch.cuda.synchronize()
+        # replay() launches on the current stream: make it the step's stream
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            same = all(torch.equal(a, b) for a, b in zip(eager, (step.y, step.dx, step.dw)))
+            for _ in range(2):
+                g.replay()
+            stream.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            t1.record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / args.steps
+        del g
+        return {"ms_per_step": round(ms, 4), "value": round(STEP_FLOPS / (ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "steps": args.steps, "identical_outputs": same}
+    except Exception as exc:  # noqa: BLE001 - reported, not fatal
+        return {"unavailable": f"{type(exc).__name__}: {str(exc)[:160]}"}
 
 
 def mma_probe(nv, clocks):
@@ -874,6 +910,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="quantise-only sweep, 2^20 .. 2^30 elements")
     ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS BF16/FP8 context timings")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 2^30-element quantise-only point")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
     ap.add_argument("--b2b", action="store_true",
                     help="with --case: also run each op back to back for ~0.6 s with clocks sampled")
     ap.add_argument("--case", action="append", default=[],
