@@ -259,9 +259,10 @@ def run_ours(args):
     clocks = clk.summary()
 
     value = job_tflops(STEP_FLOPS, ms_step, world)
-    probe = qroof = sweep = None
+    probe = qroof = sweep = delivery = None
     if rank == 0:
         probe = mma_probe(nv, clocks)
+        delivery = delivery_probe(nv, gemm_ms["fprop"], torch.cuda.get_device_properties(device).multi_processor_count)
         qroof = quant_roofline(nv, step, stream, peaks, args)
         sweep = sweep_point(nv, stream, peaks, args) if not args.no_sweep else None
     graph = graph_replay(step, stream, args) if not args.no_graph else None
@@ -289,6 +290,8 @@ def run_ours(args):
             if probe.get("tflops_at_step_clock"):
                 roofline["frac_of_probe_at_step_clock"] = round(fprop_tflops / probe["tflops_at_step_clock"], 4)
             roofline["frac_of_probe_at_max_clock"] = round(fprop_tflops / probe["tflops_at_max_clock"], 4)
+        if delivery is not None:
+            roofline["operand_delivery"] = delivery
         line = {
             "metric": "NVFP4 GEMM TFLOP/s over an MLP fwd+bwd step (quantisation included)",
             "value": round(value, 2),
@@ -409,6 +412,39 @@ def mma_probe(nv, clocks):
         r["tflops_at_step_clock"] = round(per_clk * clocks["sm_mhz"] * 1e6 / 1e12, 1)
         r["step_clock_mhz"] = clocks["sm_mhz"]
     return r
+
+
+# Bytes the GEMM's TMA and bulk copies write into one CTA's shared memory per
+# 256-wide K step: A and B boxes (128 rows x 128 B each), the CTA's A scales
+# (one 2 KiB band) and all 256 rows of B scales (two bands).
+GEMM_BYTES_PER_CTA_KSTEP = 128 * 128 + 128 * 128 + 2048 + 2 * 2048
+
+
+def gemm_delivered_bytes(M, N, K):
+    """Operand and scale bytes delivered into shared memory by one GEMM
+    launch: every 256 x 256 pair tile is two CTAs, each loading its share per
+    K step."""
+    tiles = -(-M // 256) * -(-N // 256)
+    return tiles * 2 * (K // 256) * GEMM_BYTES_PER_CTA_KSTEP
+
+
+def delivery_probe(nv, fprop_ms, sms):
+    """The GEMM's second bound: the per-SM rate at which bulk copies fill
+    shared memory (the library's delivery-rate probe, L2-resident source, all
+    SMs and a quarter of them), against the rate at which the fprop launch
+    had its operand bytes delivered."""
+    try:
+        full = nv.measure_copy_rate(32)
+        quarter = nv.measure_copy_rate(32, ctas=sms // 4)
+    except Exception as exc:  # noqa: BLE001 - reported, not fatal
+        return {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
+    d = gemm_delivered_bytes(T, F2, H)
+    per_sm = d / (fprop_ms * 1e-3) / sms / 1e9
+    need = GEMM_BYTES_PER_CTA_KSTEP / 512  # bytes per SM cycle at the full tensor rate (4 x 128-cycle MMAs)
+    return {"probe_all_sms": full, "probe_quarter_sms": quarter,
+            "fprop_delivered_bytes": d, "fprop_achieved_gbs_per_sm": round(per_sm, 1),
+            "frac_of_probe": round(per_sm / full["gbs_per_sm_median"], 4),
+            "bytes_per_sm_cycle_at_full_tensor_rate": round(need, 1)}
 
 
 def quant_roofline(nv, step, stream, peaks, args):

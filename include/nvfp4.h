@@ -233,6 +233,22 @@ int nvfp4_selftest_wait_timeout(uint32_t limit_us, nvfp4_stream_t stream);
 int nvfp4_mma_rate_probe(int32_t n_mma, int32_t mma_n, uint64_t* out, int32_t* pairs_launched,
                          nvfp4_stream_t stream);
 
+/* ---- operand delivery-rate probe ----------------------------------------- */
+/* Measure how fast global memory (L2 when src_bytes fits in it) fills one
+ * multiprocessor's shared memory by bulk asynchronous copies, the path the
+ * GEMM's operand tiles take: each of `ctas` CTAs (one per multiprocessor,
+ * 1 .. multiprocessors) streams `iters` (1 .. 2^20) 16 KiB copies from src
+ * into a 12-slot shared-memory ring, cycling through src.  src is device
+ * memory, 16-byte aligned, src_bytes >= 16384 (whole 16 KiB chunks are
+ * used).  For CTA c, out[2 c] receives the nanoseconds from its first copy
+ * to the arrival of its last (0 if a bounded wait expired) and out[2 c + 1]
+ * the bytes it received; out is device memory with room for 2 * ctas uint64
+ * values (8-byte aligned).  Not part of the pages' method: it is the
+ * measured per-multiprocessor operand delivery rate that bounds the GEMM
+ * alongside the tensor-core rate. */
+int nvfp4_copy_rate_probe(const void* src, int64_t src_bytes, int32_t ctas, int32_t iters, uint64_t* out,
+                          nvfp4_stream_t stream);
+
 /* ---- codec diagnostics (exhaustive conversion checks) -------------------- */
 /* out[i] = E2M1 code (low nibble) of v[i] with round-to-nearest-even,
  * saturating, sign kept -- the element encoder the quantiser uses.

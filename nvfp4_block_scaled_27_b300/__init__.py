@@ -47,6 +47,7 @@ EXPORTED = (
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3", "nvfp4_selftest_wait_timeout",
     "nvfp4_mma_rate_probe",
+    "nvfp4_copy_rate_probe",
 )
 
 
@@ -103,6 +104,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_selftest_wait_timeout.argtypes = [u32, vp]
     L.nvfp4_mma_rate_probe.restype = ctypes.c_int
     L.nvfp4_mma_rate_probe.argtypes = [ctypes.c_int32, ctypes.c_int32, vp, ctypes.POINTER(ctypes.c_int32), vp]
+    L.nvfp4_copy_rate_probe.restype = ctypes.c_int
+    L.nvfp4_copy_rate_probe.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp]
     L.nvfp4_encode_e2m1_rne.restype = ctypes.c_int
     L.nvfp4_encode_e2m1_rne.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e2m1_sr.restype = ctypes.c_int
@@ -275,6 +278,36 @@ def measure_mma_rate(n_mma: int = 8192, mma_n: int = 256, device=None) -> dict:
             "cycles_per_mma": round(per_mma, 2), "flop_per_sm_per_cycle": round(flop_per_sm / per_mma, 1),
             "probe_sm_ghz": round(ghz, 4), "sms": sms,
             "tflops_at_probe_clock": round(flop_per_sm / per_mma * sms * ghz * 1e9 / 1e12, 1)}
+
+
+def nvfp4_copy_rate_probe(src: torch.Tensor, ctas: int, iters: int, out: torch.Tensor, stream=None) -> None:
+    _require_cuda(src, out)
+    _check(load_library().nvfp4_copy_rate_probe(src.data_ptr(), src.numel() * src.element_size(), ctas, iters,
+                                                out.data_ptr(), _stream(stream)), "nvfp4_copy_rate_probe")
+
+
+def measure_copy_rate(src_mib: int = 32, ctas=None, iters: int = 2048, device=None) -> dict:
+    """Per-multiprocessor shared-memory fill rate of bulk copies from a
+    src_mib MiB device buffer (L2-resident at the default size), one CTA per
+    multiprocessor on `ctas` of them (all by default): the median over CTAs of
+    bytes received / time, and the whole-GPU total, in GB/s."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ctas = sms if ctas is None else int(ctas)
+    src = torch.ones(src_mib << 20, dtype=torch.uint8, device=dev)
+    out = torch.zeros(2 * ctas, dtype=torch.int64, device=dev)
+    nvfp4_copy_rate_probe(src, ctas, max(1, iters // 4), out)  # warm-up
+    nvfp4_copy_rate_probe(src, ctas, iters, out)
+    torch.cuda.synchronize(dev)
+    check_status()
+    v = out.view(-1, 2).cpu()
+    if int(v[:, 0].min()) == 0:
+        raise Nvfp4Error("copy-rate probe: a bounded wait expired")
+    rates = sorted(int(b) / int(t) for t, b in v.tolist())  # bytes per ns = GB/s
+    per_sm = rates[len(rates) // 2]
+    return {"src_mib": src_mib, "ctas": ctas, "sms": sms, "chunk_bytes": 16384, "slots": 12, "iters": iters,
+            "gbs_per_sm_median": round(per_sm, 1), "gbs_per_sm_min": round(rates[0], 1),
+            "total_tbs": round(sum(rates) / 1e3, 2)}
 
 
 def nvfp4_encode_e2m1_rne(v: torch.Tensor, out: torch.Tensor, stream=None) -> None:

@@ -739,3 +739,64 @@ int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long l
 }
 
 }  // namespace nvfp4
+
+// --------------------------------------------------- delivery-rate probe --
+// How fast bulk asynchronous copies fill one multiprocessor's shared memory,
+// the path every operand and scale byte of the GEMM takes.  Thread 0 of each
+// CTA keeps COPY_SLOTS copies of COPY_CHUNK bytes in flight, reusing a slot
+// as soon as its previous copy has landed; the data is never read.  Every
+// wait is bounded.
+namespace nvfp4 {
+namespace gemm {
+
+constexpr int COPY_CHUNK = 16384;
+constexpr int COPY_SLOTS = 12;
+constexpr int COPY_SMEM = COPY_CHUNK * COPY_SLOTS + COPY_SLOTS * 8 + 1024;
+
+__global__ void __launch_bounds__(32, 1)
+copy_rate_kernel(const uint8_t* src, int64_t nchunks, int iters, unsigned long long* out, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  if (threadIdx.x != 0) return;
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bars = ring + COPY_CHUNK * COPY_SLOTS;
+  for (int s = 0; s < COPY_SLOTS; ++s) mbar_init(bars + 8 * s, 1);
+  fence_barrier_init();
+  int64_t chunk = ((int64_t)blockIdx.x * 7919) % nchunks;  // CTAs start far apart in src
+  const uint64_t t0 = globaltimer_ns();
+  bool ok = true;
+  int issued = 0;
+  for (; issued < iters; ++issued) {
+    const int s = issued % COPY_SLOTS;
+    const uint32_t bar = bars + 8 * s;
+    if (issued >= COPY_SLOTS && !mbar_wait(bar, (uint32_t)((issued / COPY_SLOTS - 1) & 1), status)) {
+      ok = false;
+      break;
+    }
+    mbar_arrive_expect_tx(bar, COPY_CHUNK);
+    bulk_load(ring + s * COPY_CHUNK, src + chunk * COPY_CHUNK, COPY_CHUNK, bar);
+    chunk += gridDim.x;
+    if (chunk >= nchunks) chunk %= nchunks;
+  }
+  // every copy issued must land before the CTA exits, also after a timeout
+  for (int i = issued > COPY_SLOTS ? issued - COPY_SLOTS : 0; i < issued; ++i)
+    ok = mbar_wait(bars + 8 * (i % COPY_SLOTS), (uint32_t)((i / COPY_SLOTS) & 1), status) && ok;
+  const uint64_t t1 = globaltimer_ns();
+  out[2 * blockIdx.x] = ok ? t1 - t0 : 0ull;
+  out[2 * blockIdx.x + 1] = ok ? (unsigned long long)iters * COPY_CHUNK : 0ull;
+}
+
+}  // namespace gemm
+
+int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int ctas, int iters,
+                     unsigned long long* out, cudaStream_t stream) {
+  using namespace gemm;
+  if (cudaFuncSetAttribute(copy_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, COPY_SMEM) !=
+      cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  copy_rate_kernel<<<ctas, 32, COPY_SMEM, stream>>>(static_cast<const uint8_t*>(src), src_bytes / COPY_CHUNK,
+                                                   iters, out, dev.status);
+  return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4

@@ -50,6 +50,10 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
 int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long long* out, int* pairs_out,
                     cudaStream_t stream);
 
+// Operand delivery-rate probe (arguments validated by the caller).
+int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int ctas, int iters,
+                     unsigned long long* out, cudaStream_t stream);
+
 // Bounded-wait self-test.
 int selftest_wait_launch(const DeviceInfo& dev, uint64_t limit_ns, cudaStream_t stream);
 

@@ -120,6 +120,17 @@ def test_mma_rate_probe_arguments_rejected_on_host(lib):
     assert pairs.value == 0
 
 
+def test_copy_rate_probe_arguments_rejected_on_host(lib):
+    assert lib.nvfp4_copy_rate_probe(None, 1 << 20, 4, 16, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_copy_rate_probe(256, 16383, 4, 16, 16, None) == nv.ERR_INVALID_ARG  # under one chunk
+    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 0, 16, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 0, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, (1 << 20) + 1, 16, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_copy_rate_probe(264, 1 << 20, 4, 16, 16, None) == nv.ERR_INVALID_ARG  # src misaligned
+    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 16, 12, None) == nv.ERR_INVALID_ARG  # out misaligned
+    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 16, None, None) == nv.ERR_INVALID_ARG
+
+
 def test_compute_calls_refuse_cpu_tensors():
     import torch
     x = torch.zeros(16, 16, dtype=torch.bfloat16)

@@ -85,3 +85,15 @@ def test_mma_probe_scales_to_clocks():
             raise RuntimeError("no device")
 
     assert "unavailable" in bench.mma_probe(Broken, {"sm_mhz": None})
+
+
+def test_gemm_delivered_bytes_counts_tiles_ctas_and_ksteps():
+    """One 256 x 256 pair tile at K = 256 is two CTAs, each receiving an A box,
+    a B box (128 rows x 128 B each), one 2 KiB band of A scales and two of B
+    scales; ragged edges round up to whole tiles."""
+    import bench
+    per_cta = 2 * 128 * 128 + 3 * 2048
+    assert bench.GEMM_BYTES_PER_CTA_KSTEP == per_cta
+    assert bench.gemm_delivered_bytes(256, 256, 256) == 2 * per_cta
+    assert bench.gemm_delivered_bytes(257, 256, 512) == 2 * 2 * 2 * per_cta
+    assert bench.gemm_delivered_bytes(32768, 28672, 4096) == 128 * 112 * 2 * 16 * per_cta

@@ -224,3 +224,18 @@ def test_mma_rate_probe_reports_every_pair():
     assert 0.5 <= r["probe_sm_ghz"] <= 2.2, r
     r128 = nv.measure_mma_rate(2048, 128)
     assert r128["cycles_per_mma"] < r["cycles_per_mma"], (r128, r)
+
+
+def test_copy_rate_probe_reports_every_cta():
+    """The operand delivery-rate probe (the GEMM's other measured bound) runs
+    one CTA per SM; every CTA reports its bytes and time, and the rate per SM
+    is the same whether all SMs or a quarter of them stream at once (the limit
+    is per SM, not the L2 as a whole)."""
+    nv.load_library()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    full = nv.measure_copy_rate(32, iters=1024)
+    quarter = nv.measure_copy_rate(32, ctas=sms // 4, iters=1024)
+    assert full["ctas"] == sms and quarter["ctas"] == sms // 4
+    assert 20.0 <= full["gbs_per_sm_median"] <= 1000.0, full
+    assert 0.7 <= quarter["gbs_per_sm_median"] / full["gbs_per_sm_median"] <= 1.5, (quarter, full)
+
