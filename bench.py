@@ -850,7 +850,7 @@ def step_comparison(context, ms_step):
 # ------------------------------------------------------- kernel cases --
 def _parse_case(spec):
     """`gemm:M,N,K` or `quant:MODE:ROWS,COLS` (MODE in 1d, 1d_sr, 2d, 2d_t,
-    rht_t, 1d_amax_in, mx, dual_sr)."""
+    rht_t, 1d_amax_in, mx, dual_sr, dual_rne)."""
     parts = spec.split(":")
     if parts[0] == "gemm" and len(parts) == 2:
         return ("gemm", None, tuple(int(v) for v in parts[1].split(",")))
@@ -892,17 +892,18 @@ def run_cases(args):
             if mode == "1d_amax_in":
                 ain = x.abs().max().float().reshape(1)
             flags = {"1d": 0, "1d_sr": nv.ROUND_SR, "2d": nv.BLOCK_2D, "2d_t": nv.BLOCK_2D | nv.TRANSPOSE_OUT,
-                     "rht_t": nv.TRANSPOSE_OUT, "1d_amax_in": 0, "mx": 0, "dual_sr": 0}[mode]
+                     "rht_t": nv.TRANSPOSE_OUT, "1d_amax_in": 0, "mx": 0, "dual_sr": 0, "dual_rne": 0}[mode]
             if mode == "mx":
                 mc = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
                 ms = torch.empty((R, C // 32), dtype=torch.uint8, device=dev)
                 fn = (lambda x=x, mc=mc, ms=ms: nv.nvfp4_quantize_mxfp4(x, mc, ms, stream))
                 preps.append((spec, fn, (2.0 + 0.5 + 1.0 / 32.0) * R * C, "GB/s"))
                 continue
-            if mode == "dual_sr":
+            if mode in ("dual_sr", "dual_rne"):
                 oc = nv.empty_nvfp4(C, R, device=dev)
-                fn = (lambda x=x, out=out, oc=oc: nv.nvfp4_quantize_dual(x, nv.ROUND_SR, 1000, RHT_SEED, 1001, None, None,
-                                                                         out, oc, stream))
+                rr = nv.ROUND_SR if mode == "dual_sr" else nv.ROUND_RNE
+                fn = (lambda x=x, out=out, oc=oc, rr=rr: nv.nvfp4_quantize_dual(x, rr, 1000, RHT_SEED, 1001, None, None,
+                                                                                out, oc, stream))
                 preps.append((spec, fn, (2.0 + 2 * 0.5625) * R * C, "GB/s"))
                 continue
             if mode == "rht_t":
