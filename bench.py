@@ -447,14 +447,19 @@ def delivery_probe(nv, fprop_ms, sms):
     try:
         full = nv.measure_copy_rate(32)
         quarter = nv.measure_copy_rate(32, ctas=sms // 4)
+        boxes = nv.measure_copy_rate(32, mode=1)
     except Exception as exc:  # noqa: BLE001 - reported, not fatal
         return {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
     d = gemm_delivered_bytes(T, F2, H)
     per_sm = d / (fprop_ms * 1e-3) / sms / 1e9
     need = GEMM_BYTES_PER_CTA_KSTEP / 512  # bytes per SM cycle at the full tensor rate (4 x 128-cycle MMAs)
-    return {"probe_all_sms": full, "probe_quarter_sms": quarter,
+    # the busiest the tensor pipe can be kept if operands arrive no faster
+    # than the probe's boxes do (a clock-free ratio: bytes per SM cycle)
+    ceiling = boxes["bytes_per_sm_cycle_median"] / need
+    return {"tensor_active_ceiling_from_delivery": round(ceiling, 4),"probe_all_sms": full, "probe_quarter_sms": quarter, "probe_gemm_boxes": boxes,
             "fprop_delivered_bytes": d, "fprop_achieved_gbs_per_sm": round(per_sm, 1),
             "frac_of_probe": round(per_sm / full["gbs_per_sm_median"], 4),
+            "frac_of_probe_gemm_boxes": round(per_sm / boxes["gbs_per_sm_median"], 4),
             "bytes_per_sm_cycle_at_full_tensor_rate": round(need, 1)}
 
 

@@ -235,19 +235,23 @@ int nvfp4_mma_rate_probe(int32_t n_mma, int32_t mma_n, uint64_t* out, int32_t* p
 
 /* ---- operand delivery-rate probe ----------------------------------------- */
 /* Measure how fast global memory (L2 when src_bytes fits in it) fills one
- * multiprocessor's shared memory by bulk asynchronous copies, the path the
- * GEMM's operand tiles take: each of `ctas` CTAs (one per multiprocessor,
+ * multiprocessor's shared memory by asynchronous copies, the path the GEMM's
+ * operand tiles take: each of `ctas` CTAs (one per multiprocessor,
  * 1 .. multiprocessors) streams `iters` (1 .. 2^20) 16 KiB copies from src
- * into a 12-slot shared-memory ring, cycling through src.  src is device
- * memory, 16-byte aligned, src_bytes >= 16384 (whole 16 KiB chunks are
- * used).  For CTA c, out[2 c] receives the nanoseconds from its first copy
- * to the arrival of its last (0 if a bounded wait expired) and out[2 c + 1]
- * the bytes it received; out is device memory with room for 2 * ctas uint64
- * values (8-byte aligned).  Not part of the pages' method: it is the
- * measured per-multiprocessor operand delivery rate that bounds the GEMM
- * alongside the tensor-core rate. */
-int nvfp4_copy_rate_probe(const void* src, int64_t src_bytes, int32_t ctas, int32_t iters, uint64_t* out,
-                          nvfp4_stream_t stream);
+ * into a 12-slot shared-memory ring, cycling through src.  mode 0: plain
+ * bulk copies of consecutive 16 KiB chunks (src_bytes >= 16384, whole chunks
+ * used).  mode 1: the GEMM's own operand boxes, 128 rows x 128 bytes with
+ * 128-byte swizzle, through a tensor map over src viewed as rows of 2048
+ * bytes (an NVFP4 operand with K = 4096; src_bytes >= 262144, whole 128-row
+ * bands used).  src is device memory, 16-byte aligned.  For CTA c, out[3 c]
+ * receives the nanoseconds from its first copy to the arrival of its last (0
+ * if a bounded wait expired), out[3 c + 1] the bytes it received and
+ * out[3 c + 2] the SM cycles of the same interval; out is device memory with
+ * room for 3 * ctas uint64 values (8-byte aligned).  Not
+ * part of the pages' method: it is the measured per-multiprocessor operand
+ * delivery rate that bounds the GEMM alongside the tensor-core rate. */
+int nvfp4_copy_rate_probe(const void* src, int64_t src_bytes, int32_t mode, int32_t ctas, int32_t iters,
+                          uint64_t* out, nvfp4_stream_t stream);
 
 /* ---- codec diagnostics (exhaustive conversion checks) -------------------- */
 /* out[i] = E2M1 code (low nibble) of v[i] with round-to-nearest-even,

@@ -105,7 +105,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_mma_rate_probe.restype = ctypes.c_int
     L.nvfp4_mma_rate_probe.argtypes = [ctypes.c_int32, ctypes.c_int32, vp, ctypes.POINTER(ctypes.c_int32), vp]
     L.nvfp4_copy_rate_probe.restype = ctypes.c_int
-    L.nvfp4_copy_rate_probe.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp]
+    L.nvfp4_copy_rate_probe.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
     L.nvfp4_encode_e2m1_rne.restype = ctypes.c_int
     L.nvfp4_encode_e2m1_rne.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e2m1_sr.restype = ctypes.c_int
@@ -280,33 +280,42 @@ def measure_mma_rate(n_mma: int = 8192, mma_n: int = 256, device=None) -> dict:
             "tflops_at_probe_clock": round(flop_per_sm / per_mma * sms * ghz * 1e9 / 1e12, 1)}
 
 
-def nvfp4_copy_rate_probe(src: torch.Tensor, ctas: int, iters: int, out: torch.Tensor, stream=None) -> None:
+def nvfp4_copy_rate_probe(src: torch.Tensor, mode: int, ctas: int, iters: int, out: torch.Tensor,
+                          stream=None) -> None:
     _require_cuda(src, out)
-    _check(load_library().nvfp4_copy_rate_probe(src.data_ptr(), src.numel() * src.element_size(), ctas, iters,
-                                                out.data_ptr(), _stream(stream)), "nvfp4_copy_rate_probe")
+    _check(load_library().nvfp4_copy_rate_probe(src.data_ptr(), src.numel() * src.element_size(), mode, ctas,
+                                                iters, out.data_ptr(), _stream(stream)), "nvfp4_copy_rate_probe")
 
 
-def measure_copy_rate(src_mib: int = 32, ctas=None, iters: int = 2048, device=None) -> dict:
-    """Per-multiprocessor shared-memory fill rate of bulk copies from a
-    src_mib MiB device buffer (L2-resident at the default size), one CTA per
-    multiprocessor on `ctas` of them (all by default): the median over CTAs of
-    bytes received / time, and the whole-GPU total, in GB/s."""
+def measure_copy_rate(src_mib: int = 32, ctas=None, iters: int = 2048, mode: int = 0, device=None) -> dict:
+    """Per-multiprocessor shared-memory fill rate of 16 KiB asynchronous
+    copies from a src_mib MiB device buffer (L2-resident at the default
+    size), one CTA per multiprocessor on `ctas` of them (all by default):
+    mode 0 plain bulk copies, mode 1 the GEMM's swizzled 128 x 128-byte
+    operand boxes.  Returns the median over CTAs of bytes received / time,
+    and the whole-GPU total, in GB/s."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ctas = sms if ctas is None else int(ctas)
     src = torch.ones(src_mib << 20, dtype=torch.uint8, device=dev)
-    out = torch.zeros(2 * ctas, dtype=torch.int64, device=dev)
-    nvfp4_copy_rate_probe(src, ctas, max(1, iters // 4), out)  # warm-up
-    nvfp4_copy_rate_probe(src, ctas, iters, out)
+    out = torch.zeros(3 * ctas, dtype=torch.int64, device=dev)
+    nvfp4_copy_rate_probe(src, mode, ctas, max(1, iters // 4), out)  # warm-up
+    nvfp4_copy_rate_probe(src, mode, ctas, iters, out)
     torch.cuda.synchronize(dev)
     check_status()
-    v = out.view(-1, 2).cpu()
+    v = out.view(-1, 3).cpu()
     if int(v[:, 0].min()) == 0:
         raise Nvfp4Error("copy-rate probe: a bounded wait expired")
-    rates = sorted(int(b) / int(t) for t, b in v.tolist())  # bytes per ns = GB/s
+    rows = v.tolist()
+    rates = sorted(b / t for t, b, c in rows)  # bytes per ns = GB/s
+    per_clk = sorted(b / c for t, b, c in rows)  # bytes per SM cycle
+    ghz = sorted(c / t for t, b, c in rows)
     per_sm = rates[len(rates) // 2]
-    return {"src_mib": src_mib, "ctas": ctas, "sms": sms, "chunk_bytes": 16384, "slots": 12, "iters": iters,
+    return {"mode": ["bulk 16 KiB chunks", "GEMM operand boxes 128 x 128 B, 128-byte swizzle"][mode],
+            "src_mib": src_mib, "ctas": ctas, "sms": sms, "chunk_bytes": 16384, "slots": 12, "iters": iters,
             "gbs_per_sm_median": round(per_sm, 1), "gbs_per_sm_min": round(rates[0], 1),
+            "bytes_per_sm_cycle_median": round(per_clk[len(per_clk) // 2], 2),
+            "probe_sm_ghz": round(ghz[len(ghz) // 2], 4),
             "total_tbs": round(sum(rates) / 1e3, 2)}
 
 

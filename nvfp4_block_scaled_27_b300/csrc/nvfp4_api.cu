@@ -280,17 +280,18 @@ int nvfp4_mma_rate_probe(int32_t n_mma, int32_t mma_n, uint64_t* out, int32_t* p
   return rc;
 }
 
-int nvfp4_copy_rate_probe(const void* src, int64_t src_bytes, int32_t ctas, int32_t iters, uint64_t* out,
-                          nvfp4_stream_t stream) {
-  if (!src || !out || src_bytes < 16384 || iters < 1 || iters > (1 << 20) || ctas < 1)
+int nvfp4_copy_rate_probe(const void* src, int64_t src_bytes, int32_t mode, int32_t ctas, int32_t iters,
+                          uint64_t* out, nvfp4_stream_t stream) {
+  if (!src || !out || (mode != 0 && mode != 1) || iters < 1 || iters > (1 << 20) || ctas < 1)
     return NVFP4_ERR_INVALID_ARG;
+  if (src_bytes < (mode == 0 ? 16384 : 262144)) return NVFP4_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0 || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
     return NVFP4_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   int rc = check_device(&dev);
   if (rc) return rc;
   if (ctas > dev->sm_count) return NVFP4_ERR_INVALID_ARG;
-  return nvfp4::copy_rate_launch(*dev, src, src_bytes, ctas, iters, reinterpret_cast<unsigned long long*>(out),
+  return nvfp4::copy_rate_launch(*dev, src, src_bytes, mode, ctas, iters, reinterpret_cast<unsigned long long*>(out),
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 

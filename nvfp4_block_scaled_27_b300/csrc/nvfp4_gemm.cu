@@ -53,6 +53,7 @@
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 
+#include <cstring>
 #include <mutex>
 
 namespace nvfp4 {
@@ -741,20 +742,26 @@ int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long l
 }  // namespace nvfp4
 
 // --------------------------------------------------- delivery-rate probe --
-// How fast bulk asynchronous copies fill one multiprocessor's shared memory,
-// the path every operand and scale byte of the GEMM takes.  Thread 0 of each
-// CTA keeps COPY_SLOTS copies of COPY_CHUNK bytes in flight, reusing a slot
-// as soon as its previous copy has landed; the data is never read.  Every
-// wait is bounded.
+// How fast asynchronous copies fill one multiprocessor's shared memory, the
+// path every operand and scale byte of the GEMM takes.  Thread 0 of each CTA
+// keeps COPY_SLOTS copies of COPY_CHUNK bytes in flight, reusing a slot as
+// soon as its previous copy has landed; the data is never read.  kBoxes:
+// the GEMM's operand boxes (128 rows x 128 B, 128-byte swizzle) through a
+// tensor map; otherwise plain bulk copies of consecutive chunks.  Every wait
+// is bounded.
 namespace nvfp4 {
 namespace gemm {
 
 constexpr int COPY_CHUNK = 16384;
 constexpr int COPY_SLOTS = 12;
 constexpr int COPY_SMEM = COPY_CHUNK * COPY_SLOTS + COPY_SLOTS * 8 + 1024;
+constexpr int COPY_ROW_BYTES = 2048;  // box mode: src rows of an operand with K = 4096
+constexpr int COPY_BOXES_PER_BAND = COPY_ROW_BYTES / BKB;
 
+template <bool kBoxes>
 __global__ void __launch_bounds__(32, 1)
-copy_rate_kernel(const uint8_t* src, int64_t nchunks, int iters, unsigned long long* out, uint32_t* status) {
+copy_rate_kernel(const __grid_constant__ CUtensorMap map, const uint8_t* src, int64_t nchunks, int iters,
+                 unsigned long long* out, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (threadIdx.x != 0) return;
@@ -762,8 +769,10 @@ copy_rate_kernel(const uint8_t* src, int64_t nchunks, int iters, unsigned long l
   const uint32_t bars = ring + COPY_CHUNK * COPY_SLOTS;
   for (int s = 0; s < COPY_SLOTS; ++s) mbar_init(bars + 8 * s, 1);
   fence_barrier_init();
+  if (kBoxes) prefetch_tensormap(&map);
   int64_t chunk = ((int64_t)blockIdx.x * 7919) % nchunks;  // CTAs start far apart in src
   const uint64_t t0 = globaltimer_ns();
+  const unsigned long long c0 = clock64();
   bool ok = true;
   int issued = 0;
   for (; issued < iters; ++issued) {
@@ -774,7 +783,12 @@ copy_rate_kernel(const uint8_t* src, int64_t nchunks, int iters, unsigned long l
       break;
     }
     mbar_arrive_expect_tx(bar, COPY_CHUNK);
-    bulk_load(ring + s * COPY_CHUNK, src + chunk * COPY_CHUNK, COPY_CHUNK, bar);
+    if (kBoxes) {
+      const int64_t band = chunk / COPY_BOXES_PER_BAND, kb = chunk - band * COPY_BOXES_PER_BAND;
+      tma_load_2d(ring + s * COPY_CHUNK, &map, (int32_t)(kb * BKB), (int32_t)(band * BM), bar);
+    } else {
+      bulk_load(ring + s * COPY_CHUNK, src + chunk * COPY_CHUNK, COPY_CHUNK, bar);
+    }
     chunk += gridDim.x;
     if (chunk >= nchunks) chunk %= nchunks;
   }
@@ -782,20 +796,29 @@ copy_rate_kernel(const uint8_t* src, int64_t nchunks, int iters, unsigned long l
   for (int i = issued > COPY_SLOTS ? issued - COPY_SLOTS : 0; i < issued; ++i)
     ok = mbar_wait(bars + 8 * (i % COPY_SLOTS), (uint32_t)((i / COPY_SLOTS) & 1), status) && ok;
   const uint64_t t1 = globaltimer_ns();
-  out[2 * blockIdx.x] = ok ? t1 - t0 : 0ull;
-  out[2 * blockIdx.x + 1] = ok ? (unsigned long long)iters * COPY_CHUNK : 0ull;
+  const unsigned long long c1 = clock64();
+  out[3 * blockIdx.x] = ok ? t1 - t0 : 0ull;
+  out[3 * blockIdx.x + 1] = ok ? (unsigned long long)iters * COPY_CHUNK : 0ull;
+  out[3 * blockIdx.x + 2] = ok ? c1 - c0 : 0ull;
 }
 
 }  // namespace gemm
 
-int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int ctas, int iters,
+int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int mode, int ctas, int iters,
                      unsigned long long* out, cudaStream_t stream) {
   using namespace gemm;
-  if (cudaFuncSetAttribute(copy_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, COPY_SMEM) !=
-      cudaSuccess)
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  int64_t nchunks = src_bytes / COPY_CHUNK;
+  if (mode == 1) {
+    const int64_t bands = src_bytes / ((int64_t)COPY_ROW_BYTES * BM);
+    if (!make_code_map(&map, src, bands * BM, COPY_ROW_BYTES)) return NVFP4_ERR_CUDA;
+    nchunks = bands * COPY_BOXES_PER_BAND;
+  }
+  auto kernel = mode == 1 ? copy_rate_kernel<true> : copy_rate_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, COPY_SMEM) != cudaSuccess)
     return NVFP4_ERR_CUDA;
-  copy_rate_kernel<<<ctas, 32, COPY_SMEM, stream>>>(static_cast<const uint8_t*>(src), src_bytes / COPY_CHUNK,
-                                                   iters, out, dev.status);
+  kernel<<<ctas, 32, COPY_SMEM, stream>>>(map, static_cast<const uint8_t*>(src), nchunks, iters, out, dev.status);
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

@@ -51,7 +51,7 @@ int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long l
                     cudaStream_t stream);
 
 // Operand delivery-rate probe (arguments validated by the caller).
-int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int ctas, int iters,
+int copy_rate_launch(const DeviceInfo& dev, const void* src, int64_t src_bytes, int mode, int ctas, int iters,
                      unsigned long long* out, cudaStream_t stream);
 
 // Bounded-wait self-test.

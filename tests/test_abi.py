@@ -121,14 +121,22 @@ def test_mma_rate_probe_arguments_rejected_on_host(lib):
 
 
 def test_copy_rate_probe_arguments_rejected_on_host(lib):
-    assert lib.nvfp4_copy_rate_probe(None, 1 << 20, 4, 16, 16, None) == nv.ERR_INVALID_ARG
-    assert lib.nvfp4_copy_rate_probe(256, 16383, 4, 16, 16, None) == nv.ERR_INVALID_ARG  # under one chunk
-    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 0, 16, 16, None) == nv.ERR_INVALID_ARG
-    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 0, 16, None) == nv.ERR_INVALID_ARG
-    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, (1 << 20) + 1, 16, None) == nv.ERR_INVALID_ARG
-    assert lib.nvfp4_copy_rate_probe(264, 1 << 20, 4, 16, 16, None) == nv.ERR_INVALID_ARG  # src misaligned
-    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 16, 12, None) == nv.ERR_INVALID_ARG  # out misaligned
-    assert lib.nvfp4_copy_rate_probe(256, 1 << 20, 4, 16, None, None) == nv.ERR_INVALID_ARG
+    ok = (256, 1 << 20, 0, 4, 16, 16, None)
+    bad = [
+        (None, 1 << 20, 0, 4, 16, 16, None),
+        (256, 16383, 0, 4, 16, 16, None),          # under one chunk
+        (256, 262143, 1, 4, 16, 16, None),         # under one 128-row band of boxes
+        (256, 1 << 20, 2, 4, 16, 16, None),        # unknown mode
+        (256, 1 << 20, 0, 0, 16, 16, None),
+        (256, 1 << 20, 0, 4, 0, 16, None),
+        (256, 1 << 20, 0, 4, (1 << 20) + 1, 16, None),
+        (264, 1 << 20, 0, 4, 16, 16, None),        # src misaligned
+        (256, 1 << 20, 0, 4, 16, 12, None),        # out misaligned
+        (256, 1 << 20, 0, 4, 16, None, None),
+    ]
+    assert len(ok) == len(bad[0])
+    for args in bad:
+        assert lib.nvfp4_copy_rate_probe(*args) == nv.ERR_INVALID_ARG, args
 
 
 def test_compute_calls_refuse_cpu_tensors():

@@ -235,7 +235,9 @@ def test_copy_rate_probe_reports_every_cta():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     full = nv.measure_copy_rate(32, iters=1024)
     quarter = nv.measure_copy_rate(32, ctas=sms // 4, iters=1024)
-    assert full["ctas"] == sms and quarter["ctas"] == sms // 4
+    boxes = nv.measure_copy_rate(32, iters=1024, mode=1)
+    assert full["ctas"] == sms and quarter["ctas"] == sms // 4 and boxes["ctas"] == sms
     assert 20.0 <= full["gbs_per_sm_median"] <= 1000.0, full
+    assert 20.0 <= boxes["gbs_per_sm_median"] <= 1000.0, boxes
     assert 0.7 <= quarter["gbs_per_sm_median"] / full["gbs_per_sm_median"] <= 1.5, (quarter, full)
 
