@@ -25,10 +25,11 @@
 //               into a 128 x 256 fp32 accumulator in each CTA's tensor
 //               memory; tcgen05.commit multicasts stage release (`empty`)
 //               and tile completion (`tmem_full`) to both CTAs.
-//   warp 2      scale producer: the stage's scale atoms (bulk copies) into a
-//               ring of its own, refilled as soon as the scale writers have
-//               read a slot, so scales are in shared memory well before the
-//               stage's operands.
+//   warp 2      scale producer: the stage's scale atoms (A: one bulk copy;
+//               B: both bands in one 3-D TMA box) into a ring of its own,
+//               refilled as soon as the scale writers have read a slot, so
+//               scales are in shared memory well before the stage's
+//               operands.
 //   warps 3-6   scale writers, one per 32-lane tensor-memory quadrant: once
 //               the stage's scale columns are free (its previous MMAs done),
 //               copy the scale atoms from shared memory into them with
@@ -155,7 +156,8 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& tm, int
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                  const __grid_constant__ CUtensorMap tmap_c, const Params p) {
+                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sfb,
+                  const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -194,6 +196,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
     prefetch_tensormap(&tmap_c);
+    prefetch_tensormap(&tmap_sfb);
   }
   if (warp == 1) {
     tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
@@ -293,8 +296,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         tile_coords(p, t, tm, tn);
         const int band_a = 2 * tm + (int)rank;
         const bool a_ok = band_a < p.bands_a;
-        const bool b1_ok = 2 * tn + 1 < p.bands_b;
-        const uint32_t tx = (a_ok ? SFA_BYTES : 0) + SF_BAND_BYTES + (b1_ok ? SF_BAND_BYTES : 0);
+        // both bands of B scales come in one box (a missing second band reads as zeros)
+        const uint32_t tx = (a_ok ? SFA_BYTES : 0) + SFB_BYTES;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar_sf_free + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
           const uint32_t full = bar_sf_full + 8 * stage;
@@ -302,11 +305,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
           if (a_ok)
             bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
                       p.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
-          const uint8_t* sb0 = p.sfb + ((int64_t)(2 * tn) * atoms_per_band + (int64_t)kb * KSTEPS) * 512;
-          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES, sb0, SF_BAND_BYTES, full);
-          if (b1_ok)
-            bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + SF_BAND_BYTES, sb0 + atoms_per_band * 512, SF_BAND_BYTES,
-                      full);
+          tma_load_3d(sbase + OFF_SFB + stage * SFB_BYTES, &tmap_sfb, 0, kb * (SF_BAND_BYTES / 256), 2 * tn, full);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -603,6 +602,22 @@ bool make_bf16_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over B's scales in the MMA layout, viewed as [bands][K/64 atoms x
+// 2][256 bytes]: one box of (256 B, one stage's 8 pieces, 2 bands) is the
+// 4 KiB of scales a pair tile needs per K step.  Bands past the operand read
+// as zero.
+static bool make_sfb_map(CUtensorMap* map, const void* base, int64_t bands, int64_t atoms_per_band) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {256, (cuuint64_t)atoms_per_band * 2, (cuuint64_t)bands};
+  const cuuint64_t strides[2] = {256, (cuuint64_t)atoms_per_band * 512};
+  const cuuint32_t box[3] = {256, (cuuint32_t)(gemm::SF_BAND_BYTES / 256), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Map over the BF16 output [M, N] (row stride ldc elements) with 32 x 32 boxes
 // and 64-byte swizzle; stores outside [M, N] are dropped by the hardware.
 static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldc) {
@@ -650,10 +665,11 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
     }
     pairs_cap = max_pairs[dev.device];
   }
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb, tc, tsfb;
   if (!make_code_map(&ta, A.codes, A.rows, A.cols / 2)) return NVFP4_ERR_CUDA;
   if (!make_code_map(&tb, B.codes, B.rows, B.cols / 2)) return NVFP4_ERR_CUDA;
   if (!make_out_map(&tc, c, A.rows, B.rows, ldc)) return NVFP4_ERR_CUDA;
+  if (!make_sfb_map(&tsfb, B.scales, (B.rows + BM - 1) / BM, A.cols / 64)) return NVFP4_ERR_CUDA;
   Params p;
   p.sfa = A.scales;
   p.sfb = B.scales;
@@ -682,7 +698,7 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, ta, tb, tc, p) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, ta, tb, tc, tsfb, p) != cudaSuccess) return NVFP4_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
