@@ -77,25 +77,34 @@ def job_tflops(flops_per_rank_step: float, ms_per_step: float, world: int) -> fl
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clock and throttle reasons during a region.
+    Samples are taken every 20 ms from just before the region; mark() calls
+    around the region (host wall clock, after the synchronisation that ends
+    it) let summary() keep only the samples inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
+        self.window = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark(self, start: float, end: float):
+        """The region's host wall-clock bounds (time.time())."""
+        self.window = (start, end)
 
     def __exit__(self, *exc):
         self.lines = []
@@ -108,26 +117,38 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        rows = []
+        for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                rows.append((self._stamp(parts[0]), float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        if self.window is not None:
+            inside = [r for r in rows if r[0] is not None and self.window[0] <= r[0] <= self.window[1]]
+            in_window = bool(inside)
+            rows = inside or rows
+        else:
+            in_window = False
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sm = [r[1] for r in rows]
+        reasons = {n for r in rows for n, v in zip(names, r[3]) if v.lower() == "active"}
+        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": rows[-1][2], "reasons": sorted(reasons),
+                "samples": len(sm), "samples_inside_timed_region": in_window}
 
 
 class MlpStep:
@@ -229,6 +250,7 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        w0 = time.time()
         t0.record(stream)
         h0 = time.perf_counter()
         with torch.cuda.stream(stream):
@@ -237,6 +259,7 @@ def run_ours(args):
         host_ms = (time.perf_counter() - h0) * 1e3 / args.steps  # enqueue cost per step on the host
         t1.record(stream)
         stream.synchronize()
+        clk.mark(w0, time.time())
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -966,10 +989,12 @@ def _sustained(fn, stream, ms_one, work, scale, unit, seconds=0.6):
         with torch.cuda.stream(stream):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
+            w0 = time.time()
             for _ in range(n):
                 fn()
             e1.record(stream)
         stream.synchronize()
+        clk.mark(w0, time.time())
     nv.check_status(stream)
     ms = e0.elapsed_time(e1) / n
     c = clk.summary()

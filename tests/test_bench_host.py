@@ -48,20 +48,31 @@ def test_committed_traffic_figures_are_consistent():
 
 
 def test_clock_sampler_summary_parses_samples_and_reasons():
+    import datetime
     import bench
     c = bench.ClockSampler(0)
+    t = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def row(ms, rest):
+        stamp = (t + datetime.timedelta(milliseconds=ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{stamp}, {rest}"
     c.lines = [
-        "0, 210, 2032, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "0, 1905, 2032, 1050.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 1895, 2032, 1090.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 1900, 2032, 1080.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        row(0, "0, 2032, 2032, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active"),   # before the region
+        row(40, "0, 210, 2032, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        row(60, "0, 1905, 2032, 1050.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        row(80, "0, 1895, 2032, 1090.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        row(100, "0, 1900, 2032, 1080.0, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        row(300, "0, 2032, 2032, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active"),  # after it
         "garbage line",
     ]
+    c.mark(t.timestamp() + 0.03, t.timestamp() + 0.11)
     s = c.summary()
-    assert s["samples"] == 4
+    assert s["samples"] == 4 and s["samples_inside_timed_region"]
     assert s["sm_mhz"] == 1900.0  # median of the samples above half the highest (the idle one is dropped)
     assert s["sm_max_mhz"] == 2032.0
     assert s["reasons"] == ["sw_power_cap"]
+    c.window = None  # no region marked: every sample counts
+    assert c.summary()["samples"] == 6
     c.lines = []
     assert c.summary()["reasons"] == ["unsampled"]
 
