@@ -194,6 +194,22 @@ int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, 
 int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc,
                nvfp4_stream_t stream);
 
+/* Up to NVFP4_GEMM_GROUP_MAX independent GEMMs in one launch:
+ * c[i] = s_gA[i] * s_gB[i] * A[i] * B[i]^T, each exactly as nvfp4_gemm()
+ * computes it (same bits).  The backward pass of the MLP layer has two such
+ * GEMMs, dgrad and wgrad, that read different operands and write different
+ * outputs (readjensen.com NVFP4 training-recipe article, MLP data-flow
+ * paragraph).  One persistent grid shares out both problems' output tiles,
+ * longer contractions first, so neither GEMM leaves multiprocessors idle in
+ * a last partial round of tiles.  A, B, c and ldc are HOST arrays of count
+ * (1 .. NVFP4_GEMM_GROUP_MAX) entries; the tensors' buffers are device
+ * memory as for nvfp4_gemm().  Every problem is checked as nvfp4_gemm()
+ * checks it, and nothing is launched if one fails.  The outputs must not
+ * overlap each other or any operand. */
+#define NVFP4_GEMM_GROUP_MAX 2
+int nvfp4_gemm_group(int32_t count, const nvfp4_tensor* const* A, const nvfp4_tensor* const* B, void* const* c,
+                     const int64_t* ldc, nvfp4_stream_t stream);
+
 /* Synchronise `stream`, then read the device status word of the current
  * device and clear the bits it read (a bit raised meanwhile by a kernel on
  * another stream stays set for the next call).  Returns NVFP4_OK,

@@ -44,6 +44,7 @@ SCALES_MMA = 1
 EXPORTED = (
     "nvfp4_scales_bytes", "nvfp4_quantize", "nvfp4_quantize_rht_sr", "nvfp4_quantize_dual", "nvfp4_quantize_mxfp4",
     "nvfp4_gemm",
+    "nvfp4_gemm_group",
     "nvfp4_check_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_encode_e2m1_rne", "nvfp4_encode_e2m1_sr", "nvfp4_encode_e4m3", "nvfp4_selftest_wait_timeout",
     "nvfp4_mma_rate_probe",
@@ -94,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp]
     L.nvfp4_gemm.restype = ctypes.c_int
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, vp]
+    L.nvfp4_gemm_group.restype = ctypes.c_int
+    L.nvfp4_gemm_group.argtypes = [ctypes.c_int32, vp, vp, vp, vp, vp]
     L.nvfp4_check_status.restype = ctypes.c_int
     L.nvfp4_check_status.argtypes = [vp]
     L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -233,6 +236,32 @@ def nvfp4_gemm(a: NVFP4Tensor, b: NVFP4Tensor, c: torch.Tensor, stream=None) -> 
     rc = load_library().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), c.data_ptr(), c.stride(0),
                                    _stream(stream))
     _check(rc, "nvfp4_gemm")
+
+
+GEMM_GROUP_MAX = 2
+
+
+def nvfp4_gemm_group(problems, stream=None) -> None:
+    """Independent GEMMs in one launch: problems is a sequence of (a, b, c)
+    (at most GEMM_GROUP_MAX), each computed as nvfp4_gemm(a, b, c)."""
+    problems = list(problems)
+    n = len(problems)
+    if not 1 <= n <= GEMM_GROUP_MAX:
+        raise Nvfp4Error(f"a GEMM group holds 1..{GEMM_GROUP_MAX} problems")
+    for _, _, c in problems:
+        _require_cuda(c)
+        if c.dtype != torch.bfloat16 or c.dim() != 2 or c.stride(1) != 1:
+            raise Nvfp4Error("c must be a 2-D bf16 tensor with unit column stride")
+    ta = [a.c_struct() for a, _, _ in problems]
+    tb = [b.c_struct() for _, b, _ in problems]
+    pa = (ctypes.c_void_p * n)(*[ctypes.addressof(t) for t in ta])
+    pb = (ctypes.c_void_p * n)(*[ctypes.addressof(t) for t in tb])
+    pc = (ctypes.c_void_p * n)(*[c.data_ptr() for _, _, c in problems])
+    ld = (ctypes.c_int64 * n)(*[c.stride(0) for _, _, c in problems])
+    rc = load_library().nvfp4_gemm_group(n, ctypes.cast(pa, ctypes.c_void_p), ctypes.cast(pb, ctypes.c_void_p),
+                                         ctypes.cast(pc, ctypes.c_void_p), ctypes.cast(ld, ctypes.c_void_p),
+                                         _stream(stream))
+    _check(rc, "nvfp4_gemm_group")
 
 
 def nvfp4_check_status(stream=None) -> int:

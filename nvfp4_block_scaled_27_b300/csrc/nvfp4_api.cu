@@ -113,6 +113,25 @@ int quantize_common(const void* x, int64_t rows, int64_t cols, int64_t ld, uint3
   return nvfp4::quantize_launch(*dev, x, rows, cols, ld, flags, rht, rht_seed, sr_seed, amax_in, *out, s);
 }
 
+// Host-side checks of one GEMM: C[M, N] = A[M, K] * B[N, K]^T.
+int check_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, const void* c, int64_t ldc) {
+  int rc = check_tensor_buffers(A);
+  if (rc) return rc;
+  rc = check_tensor_buffers(B);
+  if (rc) return rc;
+  if (A->scale_layout != NVFP4_SCALES_MMA || B->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_INVALID_ARG;
+  const int64_t M = A->rows, N = B->rows, K = A->cols;
+  if (B->cols != K) return NVFP4_ERR_INVALID_ARG;
+  if (K % 256 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return NVFP4_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 8 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && (!c || !aligned16(c))) return NVFP4_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && K > 0 &&
+      (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales) || !aligned16(B->scales)))
+    return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,31 +217,42 @@ int nvfp4_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld, 
 }
 
 int nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* c, int64_t ldc, nvfp4_stream_t stream) {
-  int rc = check_tensor_buffers(A);
-  if (rc) return rc;
-  rc = check_tensor_buffers(B);
-  if (rc) return rc;
-  if (A->scale_layout != NVFP4_SCALES_MMA || B->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_INVALID_ARG;
-  const int64_t M = A->rows, N = B->rows, K = A->cols;
-  if (B->cols != K) return NVFP4_ERR_INVALID_ARG;
-  if (K % 256 != 0) return NVFP4_ERR_INVALID_ARG;
-  if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return NVFP4_ERR_INVALID_ARG;
-  if (ldc < N || ldc % 8 != 0) return NVFP4_ERR_INVALID_ARG;
-  if (M > 0 && N > 0 && (!c || !aligned16(c))) return NVFP4_ERR_INVALID_ARG;
-  if (M > 0 && N > 0 && K > 0 &&
-      (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales) || !aligned16(B->scales)))
-    return NVFP4_ERR_INVALID_ARG;
+  return nvfp4_gemm_group(1, &A, &B, &c, &ldc, stream);
+}
+
+int nvfp4_gemm_group(int32_t count, const nvfp4_tensor* const* A, const nvfp4_tensor* const* B, void* const* c,
+                     const int64_t* ldc, nvfp4_stream_t stream) {
+  if (count < 1 || count > NVFP4_GEMM_GROUP_MAX || !A || !B || !c || !ldc) return NVFP4_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    int rc = check_gemm(A[i], B[i], c[i], ldc[i]);
+    if (rc) return rc;
+  }
   const DeviceInfo* dev = nullptr;
-  rc = check_device(&dev);
+  int rc = check_device(&dev);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (M == 0 || N == 0) return NVFP4_OK;
-  if (K == 0) {
-    // empty contraction: C = 0
-    if (cudaMemset2DAsync(c, (size_t)ldc * 2, 0, (size_t)N * 2, (size_t)M, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-    return NVFP4_OK;
+  const nvfp4_tensor* ga[NVFP4_GEMM_GROUP_MAX];
+  const nvfp4_tensor* gb[NVFP4_GEMM_GROUP_MAX];
+  void* gc[NVFP4_GEMM_GROUP_MAX];
+  int64_t gl[NVFP4_GEMM_GROUP_MAX];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    const int64_t M = A[i]->rows, N = B[i]->rows, K = A[i]->cols;
+    if (M == 0 || N == 0) continue;
+    if (K == 0) {
+      // empty contraction: C = 0
+      if (cudaMemset2DAsync(c[i], (size_t)ldc[i] * 2, 0, (size_t)N * 2, (size_t)M, s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+      continue;
+    }
+    ga[n] = A[i];
+    gb[n] = B[i];
+    gc[n] = c[i];
+    gl[n] = ldc[i];
+    ++n;
   }
-  return nvfp4::gemm_launch(*dev, *A, *B, c, ldc, s);
+  if (n == 0) return NVFP4_OK;
+  return nvfp4::gemm_group_launch(*dev, n, ga, gb, gc, gl, s);
 }
 
 int nvfp4_check_status(nvfp4_stream_t stream) {

@@ -131,33 +131,52 @@ __device__ __forceinline__ uint32_t scale_pack2(uint32_t lo, uint32_t hi, uint64
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-struct Params {
+// One launch runs up to MAX_PROBS independent GEMMs (a group): their pair
+// tiles form one list, problem 0's first, shared out to the persistent pairs.
+constexpr int MAX_PROBS = 2;
+
+struct Prob {
   const uint8_t* sfa;  // A scales, MMA layout
   const uint8_t* sfb;  // B scales, MMA layout
   const float* sga;
   const float* sgb;
   int M, N, K;
   int bands_a, bands_b;  // 128-row scale bands present in the scale buffers
-  int tiles_m, tiles_n, num_tiles;
+  int tiles_m, tiles_n;
+  int tile0;             // index of the problem's first tile in the launch's list
+};
+
+struct Params {
+  Prob prob[MAX_PROBS];
+  int nprob;
+  int num_tiles;  // all problems
   uint32_t* status;
 };
 
-// Pair-tile order: groups of TILE_GROUP tiles along M, M fastest inside a
+// Tensor maps of every problem (grid constants, addressed per tile).
+struct Maps {
+  CUtensorMap a[MAX_PROBS], b[MAX_PROBS], c[MAX_PROBS], sfb[MAX_PROBS];
+};
+
+// Tile t of the launch: its problem (returned) and pair-tile coordinates.
+// Within a problem: groups of TILE_GROUP tiles along M, M fastest inside a
 // group, so the tiles in flight across the GPU share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(const Params& p, int t, int& tm, int& tn) {
-  const int group_span = TILE_GROUP * p.tiles_n;
-  const int g = t / group_span;
-  const int first_m = g * TILE_GROUP;
-  const int gm = min(TILE_GROUP, p.tiles_m - first_m);
-  const int r = t - g * group_span;
+__device__ __forceinline__ int tile_coords(const Params& p, int t, int& tm, int& tn) {
+  const int q = (p.nprob > 1 && t >= p.prob[1].tile0) ? 1 : 0;
+  const Prob& g = p.prob[q];
+  t -= g.tile0;
+  const int group_span = TILE_GROUP * g.tiles_n;
+  const int grp = t / group_span;
+  const int first_m = grp * TILE_GROUP;
+  const int gm = min(TILE_GROUP, g.tiles_m - first_m);
+  const int r = t - grp * group_span;
   tm = first_m + r % gm;
   tn = r / gm;
+  return q;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sfb,
-                  const Params p) {
+nvfp4_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -193,10 +212,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     mbar_init(bar_mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tensormap(&tmap_a);
-    prefetch_tensormap(&tmap_b);
-    prefetch_tensormap(&tmap_c);
-    prefetch_tensormap(&tmap_sfb);
+    for (int q = 0; q < p.nprob; ++q) {
+      prefetch_tensormap(&maps.a[q]);
+      prefetch_tensormap(&maps.b[q]);
+      prefetch_tensormap(&maps.c[q]);
+      prefetch_tensormap(&maps.sfb[q]);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(sbase + OFF_TMEM_SLOT, TMEM_COLS);
@@ -207,8 +228,6 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_kb = p.K / BK;
-  const int64_t atoms_per_band = p.K / 64;
 
   int prod_stage = 0;      // operand producer's ring position (thread 0)
   uint32_t prod_phase = 0;
@@ -220,15 +239,18 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       uint32_t& phase = prod_phase;
       for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
         int tm, tn;
-        tile_coords(p, t, tm, tn);
+        const int q = tile_coords(p, t, tm, tn);
+        const CUtensorMap* tmap_a = &maps.a[q];
+        const CUtensorMap* tmap_b = &maps.b[q];
+        const int num_kb = p.prob[q].K / BK;
         const int band_a = 2 * tm + (int)rank;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_cluster(bar_empty + 8 * stage, phase ^ 1u, p.status)) { *abort_flag = 1; break; }
           // The leader arms its barrier for both CTAs' bytes; the peer's
           // copies may land before or after that, either is fine.
           if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (A_BYTES + B_BYTES));
-          tma_load_2d_pair(sbase + OFF_A + stage * A_BYTES, &tmap_a, kb * BKB, band_a * BM, leader_full + 8 * stage);
-          tma_load_2d_pair(sbase + OFF_B + stage * B_BYTES, &tmap_b, kb * BKB, tn * BN + (int)rank * BN_CTA,
+          tma_load_2d_pair(sbase + OFF_A + stage * A_BYTES, tmap_a, kb * BKB, band_a * BM, leader_full + 8 * stage);
+          tma_load_2d_pair(sbase + OFF_B + stage * B_BYTES, tmap_b, kb * BKB, tn * BN + (int)rank * BN_CTA,
                            leader_full + 8 * stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -247,6 +269,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       int it = 0;
       bool ok = true;
       for (int t = pair; t < p.num_tiles && ok; t += num_pairs, ++it) {
+        int tm, tn;
+        const int num_kb = p.prob[tile_coords(p, t, tm, tn)].K / BK;
         // one vote keeps every lane's decision identical (waits and the
         // abort flag are read per lane)
         ok = __all_sync(0xFFFFFFFFu,
@@ -293,9 +317,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       uint32_t phase = 0;
       for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
         int tm, tn;
-        tile_coords(p, t, tm, tn);
+        const int q = tile_coords(p, t, tm, tn);
+        const Prob& g = p.prob[q];
+        const int num_kb = g.K / BK;
+        const int64_t atoms_per_band = g.K / 64;
         const int band_a = 2 * tm + (int)rank;
-        const bool a_ok = band_a < p.bands_a;
+        const bool a_ok = band_a < g.bands_a;
         // both bands of B scales come in one box (a missing second band reads as zeros)
         const uint32_t tx = (a_ok ? SFA_BYTES : 0) + SFB_BYTES;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -304,8 +331,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
           mbar_arrive_expect_tx(full, tx);
           if (a_ok)
             bulk_load(sbase + OFF_SFA + stage * SFA_BYTES,
-                      p.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
-          tma_load_3d(sbase + OFF_SFB + stage * SFB_BYTES, &tmap_sfb, 0, kb * (SF_BAND_BYTES / 256), 2 * tn, full);
+                      g.sfa + ((int64_t)band_a * atoms_per_band + (int64_t)kb * KSTEPS) * 512, SFA_BYTES, full);
+          tma_load_3d(sbase + OFF_SFB + stage * SFB_BYTES, &maps.sfb[q], 0, kb * (SF_BAND_BYTES / 256), 2 * tn, full);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -328,9 +355,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     uint32_t phase = 0;
     for (int t = pair; t < p.num_tiles && !*abort_flag; t += num_pairs) {
       int tm, tn;
-      tile_coords(p, t, tm, tn);
-      const bool a_ok = 2 * tm + (int)rank < p.bands_a;
-      const bool b1_ok = 2 * tn + 1 < p.bands_b;
+      const Prob& g = p.prob[tile_coords(p, t, tm, tn)];
+      const int num_kb = g.K / BK;
+      const bool a_ok = 2 * tm + (int)rank < g.bands_a;
+      const bool b1_ok = 2 * tn + 1 < g.bands_b;
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb) {
         // the stage's scale atoms are in shared memory, and its scale
@@ -374,8 +402,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     // --------------------------------------------------------- epilogue --
     const int quad = warp & 3;                     // lane quadrant this warp may access
     const int half = (warp - FIRST_EPI_WARP) >> 2;  // which 128 accumulator columns
-    const float alpha = __fmul_rn(*p.sga, *p.sgb);
-    const uint64_t alpha2 = f2_pack(alpha, alpha);
+    static_assert(MAX_PROBS == 2, "one alpha per problem below");
+    const float alpha_0 = __fmul_rn(*p.prob[0].sga, *p.prob[0].sgb);
+    const float alpha_1 = p.nprob > 1 ? __fmul_rn(*p.prob[1].sga, *p.prob[1].sgb) : 0.0f;
     const uint32_t leader_tmem_empty = mapa_shared(bar_tmem_empty, 0);
     const uint32_t stage_buf = sbase + OFF_EPI + (uint32_t)((warp - FIRST_EPI_WARP) * 2 * EPI_BUF_BYTES);
     const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 128);
@@ -389,7 +418,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       if (*abort_flag) break;
       tc_fence_after();
       int tm, tn;
-      tile_coords(p, t, tm, tn);
+      const int q = tile_coords(p, t, tm, tn);
+      const Prob& g = p.prob[q];
+      const float alpha = q == 0 ? alpha_0 : alpha_1;
+      const uint64_t alpha2 = f2_pack(alpha, alpha);
       // Pull this warp's 32 x 128 accumulator block out of tensor memory
       // (two 32-column loads per wait), scaling and rounding into 64 packed
       // bf16x2 words; release the accumulator as soon as the last chunk is
@@ -401,9 +433,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         tmem_ld_32x32b_x32(taddr + 32, v1);
         tc_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          w[q] = scale_pack2(v0[2 * q], v0[2 * q + 1], alpha2);
-          w[16 + q] = scale_pack2(v1[2 * q], v1[2 * q + 1], alpha2);
+        for (int j = 0; j < 16; ++j) {
+          w[j] = scale_pack2(v0[2 * j], v0[2 * j + 1], alpha2);
+          w[16 + j] = scale_pack2(v1[2 * j], v1[2 * j + 1], alpha2);
         }
         tmem_ld_32x32b_x32(taddr + 64, v0);
         tmem_ld_32x32b_x32(taddr + 96, v1);
@@ -414,17 +446,17 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          w[32 + q] = scale_pack2(v0[2 * q], v0[2 * q + 1], alpha2);
-          w[48 + q] = scale_pack2(v1[2 * q], v1[2 * q + 1], alpha2);
+        for (int j = 0; j < 16; ++j) {
+          w[32 + j] = scale_pack2(v0[2 * j], v0[2 * j + 1], alpha2);
+          w[48 + j] = scale_pack2(v1[2 * j], v1[2 * j + 1], alpha2);
         }
       }
       const int row0 = tm * BM_PAIR + (int)rank * BM + quad * 32;
       const int col0 = tn * BN + half * 128;
-      if (row0 >= p.M) continue;
+      if (row0 >= g.M) continue;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        if (col0 + EPI_BOX * ch >= p.N) break;
+        if (col0 + EPI_BOX * ch >= g.N) break;
         const uint32_t buf = stage_buf + (uint32_t)((ch & 1) * EPI_BUF_BYTES);
         // the store that last used this buffer must have read it
         if (lane == 0) {
@@ -441,7 +473,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmap_c, buf, col0 + EPI_BOX * ch, row0);
+          tma_store_2d(&maps.c[q], buf, col0 + EPI_BOX * ch, row0);
           bulk_commit_group();
         }
       }
@@ -632,9 +664,14 @@ static bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int
          CUDA_SUCCESS;
 }
 
-int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c, int64_t ldc,
-                cudaStream_t stream) {
+// Launch the GEMMs of a group (1 .. MAX_PROBS problems, each with M, N, K
+// > 0, validated by the caller) as one persistent grid.  Problems with longer
+// contractions go first in the tile list, so the pairs' last tiles are the
+// short ones.
+int gemm_group_launch(const DeviceInfo& dev, int count, const nvfp4_tensor* const* A, const nvfp4_tensor* const* B,
+                      void* const* c, const int64_t* ldc, cudaStream_t stream) {
   using namespace gemm;
+  if (count < 1 || count > MAX_PROBS) return NVFP4_ERR_INVALID_ARG;
   static std::mutex mu;
   static int max_pairs[64] = {};
   int pairs_cap = 0;
@@ -665,26 +702,43 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
     }
     pairs_cap = max_pairs[dev.device];
   }
-  CUtensorMap ta, tb, tc, tsfb;
-  if (!make_code_map(&ta, A.codes, A.rows, A.cols / 2)) return NVFP4_ERR_CUDA;
-  if (!make_code_map(&tb, B.codes, B.rows, B.cols / 2)) return NVFP4_ERR_CUDA;
-  if (!make_out_map(&tc, c, A.rows, B.rows, ldc)) return NVFP4_ERR_CUDA;
-  if (!make_sfb_map(&tsfb, B.scales, (B.rows + BM - 1) / BM, A.cols / 64)) return NVFP4_ERR_CUDA;
+  int order[MAX_PROBS];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  if (count == 2 && A[1]->cols > A[0]->cols) {
+    order[0] = 1;
+    order[1] = 0;
+  }
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
   Params p;
-  p.sfa = A.scales;
-  p.sfb = B.scales;
-  p.sga = A.global_scale;
-  p.sgb = B.global_scale;
-  p.M = (int)A.rows;
-  p.N = (int)B.rows;
-  p.K = (int)A.cols;
-  p.bands_a = (p.M + BM - 1) / BM;
-  p.bands_b = (p.N + BM - 1) / BM;
-  p.tiles_m = (p.M + BM_PAIR - 1) / BM_PAIR;
-  p.tiles_n = (p.N + BN - 1) / BN;
-  p.num_tiles = p.tiles_m * p.tiles_n;
+  memset(&p, 0, sizeof(p));
+  int tiles = 0;
+  for (int k = 0; k < count; ++k) {
+    const nvfp4_tensor& a = *A[order[k]];
+    const nvfp4_tensor& b = *B[order[k]];
+    if (!make_code_map(&maps.a[k], a.codes, a.rows, a.cols / 2)) return NVFP4_ERR_CUDA;
+    if (!make_code_map(&maps.b[k], b.codes, b.rows, b.cols / 2)) return NVFP4_ERR_CUDA;
+    if (!make_out_map(&maps.c[k], c[order[k]], a.rows, b.rows, ldc[order[k]])) return NVFP4_ERR_CUDA;
+    if (!make_sfb_map(&maps.sfb[k], b.scales, (b.rows + BM - 1) / BM, a.cols / 64)) return NVFP4_ERR_CUDA;
+    Prob& g = p.prob[k];
+    g.sfa = a.scales;
+    g.sfb = b.scales;
+    g.sga = a.global_scale;
+    g.sgb = b.global_scale;
+    g.M = (int)a.rows;
+    g.N = (int)b.rows;
+    g.K = (int)a.cols;
+    g.bands_a = (g.M + BM - 1) / BM;
+    g.bands_b = (g.N + BM - 1) / BM;
+    g.tiles_m = (g.M + BM_PAIR - 1) / BM_PAIR;
+    g.tiles_n = (g.N + BN - 1) / BN;
+    g.tile0 = tiles;
+    tiles += g.tiles_m * g.tiles_n;
+  }
+  p.nprob = count;
+  p.num_tiles = tiles;
   p.status = dev.status;
-  const int pairs = p.num_tiles < pairs_cap ? p.num_tiles : pairs_cap;
+  const int pairs = tiles < pairs_cap ? tiles : pairs_cap;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr;
@@ -698,8 +752,15 @@ int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, ta, tb, tc, tsfb, p) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, maps, p) != cudaSuccess) return NVFP4_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c, int64_t ldc,
+                cudaStream_t stream) {
+  const nvfp4_tensor* a = &A;
+  const nvfp4_tensor* b = &B;
+  return gemm_group_launch(dev, 1, &a, &b, &c, &ldc, stream);
 }
 
 }  // namespace nvfp4

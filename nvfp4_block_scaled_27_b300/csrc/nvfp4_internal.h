@@ -42,9 +42,12 @@ int quantize_dual_launch(const DeviceInfo& dev, const void* x, int64_t rows, int
 int quantize_mx_launch(const DeviceInfo& dev, const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
                        uint8_t* scales, cudaStream_t stream);
 
-// GEMM entry (arguments validated by the caller).
+// GEMM entries (arguments validated by the caller): one GEMM, or a group of
+// independent GEMMs (count 1 or 2, every M, N, K > 0) in one launch.
 int gemm_launch(const DeviceInfo& dev, const nvfp4_tensor& A, const nvfp4_tensor& B, void* c,
                 int64_t ldc, cudaStream_t stream);
+int gemm_group_launch(const DeviceInfo& dev, int count, const nvfp4_tensor* const* A, const nvfp4_tensor* const* B,
+                      void* const* c, const int64_t* ldc, cudaStream_t stream);
 
 // FP4 MMA-rate probe (arguments validated by the caller).
 int mma_rate_launch(const DeviceInfo& dev, int n_mma, int mma_n, unsigned long long* out, int* pairs_out,

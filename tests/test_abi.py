@@ -84,6 +84,26 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_gemm(ctypes.byref(b), ctypes.byref(b), 16, 64, None) == nv.ERR_INVALID_ARG
 
 
+def test_gemm_group_arguments_rejected_on_host(lib):
+    """Count out of range, null arrays, and one bad problem among good ones:
+    nothing is launched (no device is needed to reach these rejections)."""
+    good = nv.CTensor(16, 16, 16, 16, 128, 256, nv.SCALES_MMA, 0)
+    bad = nv.CTensor(16, 16, 16, 16, 128, 256, nv.SCALES_CANONICAL, 0)
+    P = ctypes.c_void_p
+    a = (P * 2)(ctypes.addressof(good), ctypes.addressof(good))
+    b = (P * 2)(ctypes.addressof(good), ctypes.addressof(bad))
+    c = (P * 2)(16, 16)
+    ld = (ctypes.c_int64 * 2)(128, 128)
+    cast = lambda arr: ctypes.cast(arr, P)  # noqa: E731
+    assert lib.nvfp4_gemm_group(0, cast(a), cast(a), cast(c), cast(ld), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_group(3, cast(a), cast(a), cast(c), cast(ld), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_group(2, None, cast(a), cast(c), cast(ld), None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_group(2, cast(a), cast(a), cast(c), None, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_group(2, cast(a), cast(b), cast(c), cast(ld), None) == nv.ERR_INVALID_ARG  # 2nd bad
+    with pytest.raises(nv.Nvfp4Error):
+        nv.nvfp4_gemm_group([])
+
+
 def test_dual_and_mxfp4_arguments_rejected_on_host(lib):
     row = nv.CTensor(1, 1, 1, 1, 64, 256, nv.SCALES_MMA, 0)
     col = nv.CTensor(1, 1, 1, 1, 256, 64, nv.SCALES_MMA, 0)
