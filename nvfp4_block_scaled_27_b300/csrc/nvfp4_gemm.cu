@@ -10,7 +10,10 @@
 // readjensen.com NVFP4 training-recipe article, MLP data-flow paragraph.
 //
 // Design: clusters of two CTAs (one per SM) work as a pair on 256 x 256
-// output tiles, persistently.  CTA r of the pair owns output rows
+// output tiles, persistently.  A launch may hold two independent problems
+// (the backward pass's dgrad and wgrad): their tiles form one list, longer
+// contraction first, and each warp looks up its tile's problem.  CTA r of
+// the pair owns output rows
 // [128 r, 128 r + 128) of the tile.  Per 256-wide K step each CTA loads 128
 // rows of A and 128 of the 256 rows of B (so each SM streams half the B bytes
 // a single-SM 128 x 256 tile would need), its own A scales and all of B's
