@@ -275,13 +275,9 @@ def run_ours(args):
     ms_step = ms / args.steps
     # Per-call times come from a second pass of K steps with CUDA events
     # around every call, kept out of the timed region above so the events do
-    # not add to the step time.  It starts after a second of idle time and a
-    # warm-up, so the GPU's clock and temperature start from where the timed
-    # region's did rather than from the end of it.
-    time.sleep(1.0)
+    # not add to the step time.  It follows the timed region at once: an idle
+    # pause before it (tried) lets the clocks drop and made every call slower.
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step.run(stream)
         for k in range(args.steps):
             step.run(stream, gemm_ev[k], quant_ev[k])
     stream.synchronize()
