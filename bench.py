@@ -480,14 +480,6 @@ def gemm_delivered_bytes(M, N, K):
     return tiles * 2 * (K // 256) * GEMM_BYTES_PER_CTA_KSTEP
 
 
-def delivery_tflops_ceiling(gbs_per_sm, sms):
-    """The GEMM FLOP rate that operands delivered at gbs_per_sm per SM would
-    sustain: one CTA's K step brings GEMM_BYTES_PER_CTA_KSTEP bytes for
-    2 x 128 x 256 x 256 flop (its 128 x 256 outputs over 256 of K)."""
-    flop_per_byte = 2.0 * 128 * 256 * 256 / GEMM_BYTES_PER_CTA_KSTEP
-    return gbs_per_sm * 1e9 * sms * flop_per_byte / 1e12
-
-
 def delivery_probe(nv, fprop_ms, sms):
     """The GEMM's second bound: the per-SM rate at which bulk copies fill
     shared memory (the library's delivery-rate probe, L2-resident source, all
@@ -505,11 +497,10 @@ def delivery_probe(nv, fprop_ms, sms):
     # the busiest the tensor pipe can be kept if operands arrive no faster
     # than the probe's boxes do (a clock-free ratio: bytes per SM cycle)
     ceiling = boxes["bytes_per_sm_cycle_median"] / need
-    tflops_ceiling = delivery_tflops_ceiling(boxes["gbs_per_sm_median"], sms)
-    fprop_tflops = 2.0 * T * F2 * H / (fprop_ms * 1e-3) / 1e12
+    # Per second the probe and the GEMM run at different clocks (the probe's
+    # rate in bytes per SM cycle is the same from 1.3 to 1.9 GHz), so the
+    # per-second ratios below depend on the box's clock state.
     return {"tensor_active_ceiling_from_delivery": round(ceiling, 4),
-            "tflops_ceiling_from_delivery": round(tflops_ceiling, 1),
-            "frac_of_delivery_ceiling": round(fprop_tflops / tflops_ceiling, 4),
             "probe_all_sms": full, "probe_quarter_sms": quarter, "probe_gemm_boxes": boxes,
             "fprop_delivered_bytes": d, "fprop_achieved_gbs_per_sm": round(per_sm, 1),
             "frac_of_probe": round(per_sm / full["gbs_per_sm_median"], 4),

@@ -108,12 +108,3 @@ def test_gemm_delivered_bytes_counts_tiles_ctas_and_ksteps():
     assert bench.gemm_delivered_bytes(256, 256, 256) == 2 * per_cta
     assert bench.gemm_delivered_bytes(257, 256, 512) == 2 * 2 * 2 * per_cta
     assert bench.gemm_delivered_bytes(32768, 28672, 4096) == 128 * 112 * 2 * 16 * per_cta
-
-
-def test_delivery_ceiling_closed_form():
-    """38,912 bytes per CTA K step feed 2 x 128 x 256 x 256 flop, so 100 GB/s on
-    each of 148 SMs sustains 148e11 x 16777216 / 38912 flop/s."""
-    import bench
-    assert abs(bench.delivery_tflops_ceiling(100.0, 148) - 148e11 * 16777216 / 38912 / 1e12) < 1e-9
-    assert abs(bench.delivery_tflops_ceiling(116.2, 148) - 7414.9) < 0.1
-
